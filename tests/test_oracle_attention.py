@@ -1,0 +1,209 @@
+"""Pins for the oracle's attention core (CPU only).
+
+The oracle is checked against things other than itself:
+  * a library routine: torch's scaled_dot_product_attention in float64 on CPU;
+  * closed forms: constant V, Q = 0, scale = 0, one key, two keys (a logistic
+    weight), -Inf logits, NaN and +Inf propagation;
+  * invariants: joint permutation of K/V rows, BSHD vs BHSD, weights summing to 1;
+  * planted mistakes: a few plausible bugs, planted in a copy of the oracle here
+    on the CPU, must each fail one of the pins above.
+Sources: snilld.dk article "Open source attention-kernel i HIP slaar AITER v3 paa
+MI300X", sections "Hvordan kernen arbejder" (softmax(QK^T/sqrt(d))V) and
+"Hvad er udgivet" (layouts, lengths, cross-attention).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import attention_fp64, attention_rows_fp64, round_bf16
+
+from bf16_forward_attention_gb300 import inputs
+
+
+def _rand(shape, seed, std=1.0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape) * std
+    # bf16-exact values, like the real inputs
+    return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _sdpa(q, k, v, scale):
+    qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(a)) for a in (q, k, v))
+    return torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale).numpy()
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,d", [(1, 1, 1, 1, 128), (2, 3, 17, 29, 128),
+                                         (1, 2, 130, 7, 128), (1, 1, 5, 300, 64)])
+def test_matches_torch_sdpa(B, H, Sq, Sk, d):
+    q, k, v = _rand((B, H, Sq, d), 1), _rand((B, H, Sk, d), 2), _rand((B, H, Sk, d), 3)
+    scale = inputs.default_scale(d)
+    got = attention_fp64(q, k, v, scale)
+    want = _sdpa(q, k, v, float(np.float32(scale)))
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_wide_logits_match_sdpa():
+    q, k = _rand((1, 2, 9, 128), 4, 8.0), _rand((1, 2, 33, 128), 5, 8.0)
+    v = _rand((1, 2, 33, 128), 6)
+    scale = inputs.default_scale()
+    np.testing.assert_allclose(attention_fp64(q, k, v, scale),
+                               _sdpa(q, k, v, float(np.float32(scale))), rtol=1e-11, atol=1e-12)
+
+
+def test_constant_v_gives_v():
+    q, k = _rand((1, 2, 11, 128), 7), _rand((1, 2, 13, 128), 8)
+    c = _rand((128,), 9)
+    v = np.broadcast_to(c, (1, 2, 13, 128)).copy()
+    o = attention_fp64(q, k, v, 0.088)
+    np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), rtol=1e-14, atol=0)
+    for mode in ("rtne", "rtna"):  # the fp64 result is within 1e-14 of a bf16 value
+        assert (round_bf16(o, mode) == round_bf16(np.broadcast_to(c, o.shape), mode)).all()
+
+
+def test_zero_q_and_zero_scale_give_mean():
+    k, v = _rand((1, 1, 19, 128), 10), _rand((1, 1, 19, 128), 11)
+    mean = v.mean(axis=2, keepdims=True)
+    o = attention_fp64(np.zeros((1, 1, 4, 128)), k, v, 0.5)
+    np.testing.assert_allclose(o, np.broadcast_to(mean, o.shape), rtol=1e-13, atol=1e-15)
+    o = attention_fp64(_rand((1, 1, 4, 128), 12), k, v, 0.0)
+    np.testing.assert_allclose(o, np.broadcast_to(mean, o.shape), rtol=1e-13, atol=1e-15)
+
+
+def test_single_key_gives_v0():
+    q, k, v = _rand((1, 1, 6, 128), 13), _rand((1, 1, 1, 128), 14), _rand((1, 1, 1, 128), 15)
+    o = attention_fp64(q, k, v, 0.3)
+    assert (o == np.broadcast_to(v, o.shape)).all()
+
+
+def test_two_keys_logistic_closed_form():
+    # s0 - s1 = scale * q.(k0 - k1); the weight of key 0 is 1 / (1 + exp(-(s0 - s1))).
+    rng = np.random.default_rng(16)
+    for _ in range(20):
+        q, k, v = _rand((1, 1, 1, 128), rng.integers(1e9)), _rand((1, 1, 2, 128), rng.integers(1e9)), \
+            _rand((1, 1, 2, 128), rng.integers(1e9))
+        scale = float(np.float32(rng.uniform(-0.3, 0.3)))
+        ds = scale * math.fsum(q[0, 0, 0] * (k[0, 0, 0] - k[0, 0, 1]))
+        w0 = 1.0 / (1.0 + math.exp(-ds))
+        want = w0 * v[0, 0, 0] + (1.0 - w0) * v[0, 0, 1]
+        np.testing.assert_allclose(attention_fp64(q, k, v, scale)[0, 0, 0], want,
+                                   rtol=1e-12, atol=1e-14)
+
+
+def test_weights_sum_to_one():
+    # With V = identity rows, O_i is the softmax row itself.
+    Sk = 40
+    q, k = _rand((1, 1, 8, 128), 17), _rand((1, 1, Sk, 128), 18)
+    v = np.zeros((1, 1, Sk, 128))
+    v[0, 0, np.arange(Sk), np.arange(Sk)] = 1.0
+    o = attention_fp64(q, k, v, inputs.default_scale())
+    np.testing.assert_allclose(o.sum(axis=-1), 1.0, rtol=0, atol=1e-15)
+    assert (o[..., Sk:] == 0).all() and (o[..., :Sk] > 0).all()
+
+
+def test_joint_kv_permutation_invariance():
+    q, k, v = _rand((1, 2, 10, 128), 19), _rand((1, 2, 50, 128), 20), _rand((1, 2, 50, 128), 21)
+    perm = np.random.default_rng(22).permutation(50)
+    a = attention_fp64(q, k, v, 0.09)
+    b = attention_fp64(q, k[:, :, perm], v[:, :, perm], 0.09)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-15)
+
+
+def test_layouts_agree():
+    q, k, v = _rand((2, 3, 9, 128), 23), _rand((2, 3, 14, 128), 24), _rand((2, 3, 14, 128), 25)
+    a = attention_fp64(q, k, v, 0.1, "bhsd")
+    t = lambda x: np.ascontiguousarray(np.swapaxes(x, 1, 2))
+    b = attention_fp64(t(q), t(k), t(v), 0.1, "bshd")
+    assert (t(a) == b).all()
+
+
+def test_rows_subset_matches_full():
+    q, k, v = _rand((1, 1, 37, 128), 26), _rand((1, 1, 41, 128), 27), _rand((1, 1, 41, 128), 28)
+    full = attention_fp64(q, k, v, 0.1)[0, 0]
+    rows = [0, 5, 36]
+    sub = attention_rows_fp64(q[0, 0], k[0, 0], v[0, 0], 0.1, rows)
+    assert (sub == full[rows]).all()
+
+
+def test_nan_in_q_row_gives_nan_row_only():
+    q, k, v = _rand((1, 1, 6, 128), 29), _rand((1, 1, 9, 128), 30), _rand((1, 1, 9, 128), 31)
+    q[0, 0, 2, 77] = np.nan
+    o = attention_fp64(q, k, v, 0.1)
+    assert np.isnan(o[0, 0, 2]).all()
+    assert np.isfinite(np.delete(o[0, 0], 2, axis=0)).all()
+
+
+def test_inf_in_k_closed_form():
+    # One +Inf at K[j, c]: s_ij = +Inf if q_ic > 0 (row NaN: Inf - Inf), NaN if q_ic = 0
+    # (0 * Inf), -Inf if q_ic < 0 (key j gets weight exp(-Inf) = 0).
+    q, k, v = _rand((1, 1, 64, 128), 32), _rand((1, 1, 9, 128), 33), _rand((1, 1, 9, 128), 34)
+    j, c = 4, 50
+    q[0, 0, :3, c] = [0.0, -0.0, 1.0]
+    q[0, 0, 3, c] = -2.0
+    k[0, 0, j, c] = np.inf
+    o = attention_fp64(q, k, v, 0.1)[0, 0]
+    nan_rows = q[0, 0, :, c] >= 0
+    assert np.isnan(o[nan_rows]).all()
+    assert np.isfinite(o[~nan_rows]).all()
+    keep = [i for i in range(9) if i != j]
+    ref = attention_fp64(q[:, :, ~nan_rows], k[:, :, keep], v[:, :, keep], 0.1)[0, 0]
+    np.testing.assert_allclose(o[~nan_rows], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_all_minus_inf_row_is_nan():
+    q = np.ones((1, 1, 1, 128))
+    k = np.full((1, 1, 3, 128), -np.inf)
+    v = _rand((1, 1, 3, 128), 35)
+    assert np.isnan(attention_fp64(q, k, v, 0.1)).all()
+
+
+def test_generator_is_deterministic_and_shaped():
+    w = inputs.WORKLOADS["tiny"].scaled(Sq=5, Sk=7, H=1)
+    a = inputs.make_qkv(w)
+    b = inputs.make_qkv(w)
+    assert all(torch.equal(x.view(torch.int16), y.view(torch.int16)) for x, y in zip(a, b))
+    assert a[0].shape == (1, 1, 5, 128) and a[1].shape == (1, 1, 7, 128)
+    s = inputs.normal_f32(1, 0, 200000)
+    assert abs(s.mean()) < 0.01 and abs(s.std() - 1) < 0.01
+    u = inputs.uniform_f32(1, 1, 200000, -1, 1)
+    assert u.min() >= -1 and u.max() < 1 and abs(u.mean()) < 0.01
+
+
+# --- planted mistakes: each must be caught by a pin above -----------------------
+
+def _mutant(kind):
+    def rows(q, k, v, scale, rows=None):
+        scale_d = float(np.float32(scale))
+        if rows is not None:
+            q = q[np.asarray(rows)]
+        if kind == "no_scale":
+            s = q @ k.T
+        elif kind == "transposed_v":
+            s = (q @ k.T) * scale_d
+        else:
+            s = (q @ k.T) * scale_d
+        m = np.max(s, axis=1, keepdims=True)
+        p = np.exp(s - m)
+        l = np.sum(p, axis=1, keepdims=True)
+        if kind == "no_normalise":
+            return p @ v
+        if kind == "wrong_axis":
+            return (p / p.sum(axis=0, keepdims=True)) @ v
+        if kind == "transposed_v":
+            vv = v.T if v.shape[0] == v.shape[1] else v[::-1]
+            return p @ vv / l
+        return p @ v / l
+    return rows
+
+
+@pytest.mark.parametrize("kind", ["no_scale", "no_normalise", "wrong_axis", "transposed_v"])
+def test_planted_mistakes_are_caught(kind, monkeypatch):
+    import oracle.attention as oa
+    monkeypatch.setattr(oa, "attention_rows_fp64", _mutant(kind))
+    q, k, v = _rand((1, 1, 17, 128), 36), _rand((1, 1, 29, 128), 37), _rand((1, 1, 29, 128), 38)
+    scale = inputs.default_scale()
+    got = oa.attention_fp64(q, k, v, scale)
+    want = _sdpa(q, k, v, float(np.float32(scale)))
+    assert not np.allclose(got, want, rtol=1e-12, atol=1e-13)
