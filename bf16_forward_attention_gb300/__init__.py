@@ -1,0 +1,132 @@
+"""GB300-native bf16 forward attention.
+
+The product is the C ABI in ``include/attn_fwd.h`` (library
+``_lib/libattn_fwd.so``, built by ``build.py``). This module is the thin Python
+binding: it checks tensors, marshals pointers and sizes, and calls the library on
+the current torch stream. Every step of the computation runs in the CUDA kernel;
+there is no Python or CPU fallback - if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from .build import LIB_PATH
+
+LAYOUTS = {"bhsd": 0, "bshd": 1}
+ROUNDINGS = {"rtne": 0, "rtna": 1, "rtz": 2}
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_MISALIGNED = -3
+ATTN_ERR_ALIASING = -4
+ATTN_ERR_NO_DEVICE = -5
+ATTN_ERR_ARCH = -6
+ATTN_ERR_LAUNCH = -7
+ATTN_ERR_TIMEOUT = -8
+ATTN_ERR_TOO_LARGE = -9
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A nonzero status from the C library."""
+
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"attn_fwd failed ({status}): {msg}")
+        self.status = status
+
+
+def load_library() -> ctypes.CDLL:
+    """Load ``libattn_fwd.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"CUDA library not built: {LIB_PATH} is missing. "
+            "Run `python -m bf16_forward_attention_gb300.build` (needs nvcc).")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64 = ctypes.c_int64
+    lib.attn_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64, i64, i64,
+                                                     ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
+    lib.attn_fwd.restype = ctypes.c_int
+    lib.attn_status_str.argtypes = [ctypes.c_int]
+    lib.attn_status_str.restype = ctypes.c_char_p
+    lib.attn_fwd_last_error.argtypes = []
+    lib.attn_fwd_last_error.restype = ctypes.c_int
+    lib.attn_fwd_version.argtypes = []
+    lib.attn_fwd_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load_library().attn_status_str(int(status)).decode()
+
+
+def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, B: int, H: int,
+                 Sq: int, Sk: int, d: int, scale: float, rounding_mode: int, stream: int) -> int:
+    """Direct call of the C entry point ``attn_fwd``; returns its status code."""
+    return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq, Sk, d,
+                                   ctypes.c_float(scale), rounding_mode, stream)
+
+
+def attn_fwd_last_error() -> int:
+    return load_library().attn_fwd_last_error()
+
+
+def _dims(x, layout):
+    if layout == "bhsd":
+        B, H, S, D = x.shape
+    else:
+        B, S, H, D = x.shape
+    return B, H, S, D
+
+
+def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
+             rounding: str = "rtne", out=None):
+    """O = softmax(Q K^T * scale) V on bf16 CUDA tensors (head_dim 128).
+
+    q: (B, H, Sq, 128) for "bhsd" or (B, Sq, H, 128) for "bshd"; k, v likewise with
+    Sk. Returns ``out`` (allocated like q if not given) in the same layout, rounded
+    to bf16 per ``rounding`` ("rtne", "rtna", "rtz"). Runs on the current stream.
+    """
+    import torch
+
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(LAYOUTS)}")
+    if rounding not in ROUNDINGS:
+        raise ValueError(f"rounding must be one of {sorted(ROUNDINGS)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, H, Sq, D = _dims(q, layout)
+    Bk, Hk, Sk, Dk = _dims(k, layout)
+    if (Bk, Hk, Dk) != (B, H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+    if out is None:
+        out = torch.empty_like(q)
+    elif (out.dtype != torch.bfloat16 or out.shape != q.shape or not out.is_contiguous()
+          or out.device != q.device):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          LAYOUTS[layout], B, H, Sq, Sk, D, float(scale), ROUNDINGS[rounding],
+                          stream)
+    if st != ATTN_OK:
+        raise AttnError(st, status_str(st))
+    return out
+
+
+__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "status_str", "load_library",
+           "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

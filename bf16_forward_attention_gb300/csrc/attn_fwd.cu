@@ -1,0 +1,191 @@
+// attn_fwd.cu - host side of the C ABI declared in include/attn_fwd.h.
+//
+// Validates the call on the host, builds the four TMA tensor maps (Q, K, V, O;
+// the layout only changes their strides and coordinate order, so both BSHD and
+// BHSD are read in place), sizes the grid (one CTA per pair of 128-row query
+// tiles of one (batch, head), consecutive CTAs on the same head so that K/V
+// stay in L2) and launches the kernel on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_fwd.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxDevices = 64;
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+std::mutex g_dev_mutex;
+int g_dev_state[kMaxDevices];  // 0 = not set up, 1 = ready, negative = status to return
+
+// Once per device: check the architecture and raise the shared-memory limit.
+int device_ready(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_dev_state[dev] != 0) return g_dev_state[dev] > 0 ? ATTN_OK : g_dev_state[dev];
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (major != 10 || minor != 3) {
+    g_dev_state[dev] = ATTN_ERR_ARCH;
+    return ATTN_ERR_ARCH;
+  }
+  if (cudaFuncSetAttribute(attn::attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           attn::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  g_dev_state[dev] = 1;
+  return ATTN_OK;
+}
+
+// 4-D map over a (B, H, S, 128) bf16 tensor in the given layout, box of
+// 64 columns x box_rows rows, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* map, const void* ptr, int layout, int64_t B, int64_t H, int64_t S,
+              uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t row = 128 * 2;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (layout == ATTN_LAYOUT_BHSD) {
+    dims[0] = 128; dims[1] = S; dims[2] = H; dims[3] = B;
+    strides[0] = row; strides[1] = S * row; strides[2] = H * S * row;
+    box[0] = 64; box[1] = box_rows; box[2] = 1; box[3] = 1;
+  } else {
+    dims[0] = 128; dims[1] = H; dims[2] = S; dims[3] = B;
+    strides[0] = row; strides[1] = H * row; strides[2] = S * H * row;
+    box[0] = 64; box[1] = 1; box[2] = box_rows; box[3] = 1;
+  }
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_str(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, size < 1 or non-finite scale)";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported (head_dim must be 128; unknown layout or rounding mode)";
+    case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ATTN_ERR_ALIASING: return "output overlaps an input";
+    case ATTN_ERR_NO_DEVICE: return "no usable CUDA device";
+    case ATTN_ERR_ARCH: return "device is not compute capability 10.3 (sm_103)";
+    case ATTN_ERR_LAUNCH: return "CUDA launch or tensor-map setup failed";
+    case ATTN_ERR_TIMEOUT: return "a device-side wait timed out";
+    case ATTN_ERR_TOO_LARGE: return "size beyond tensor-map or grid limits";
+    default: return "unknown status";
+  }
+}
+
+int attn_fwd_version(void) { return kVersion; }
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
+             int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
+             void* stream) {
+  // ---- host-side validation (nothing is launched on failure)
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (layout != ATTN_LAYOUT_BHSD && layout != ATTN_LAYOUT_BSHD) return ATTN_ERR_UNSUPPORTED;
+  if (rounding_mode < ATTN_ROUND_RTNE || rounding_mode > ATTN_ROUND_RTZ) return ATTN_ERR_UNSUPPORTED;
+  // TMA: coordinates are int32, strides < 2^40 bytes; grid.x < 2^31.
+  const int64_t kLim31 = (int64_t(1) << 31) - 1;
+  if (Sq > kLim31 || Sk > kLim31 || H > kLim31 || B > kLim31) return ATTN_ERR_TOO_LARGE;
+  const int64_t kStrideLim = int64_t(1) << 40;
+  if (H > kStrideLim / 256 / Sq || H > kStrideLim / 256 / Sk) return ATTN_ERR_TOO_LARGE;
+  if (B > (int64_t(1) << 62) / 256 / H / (Sq > Sk ? Sq : Sk)) return ATTN_ERR_TOO_LARGE;
+  const int64_t n_qpairs = (Sq + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  if (B * H > kLim31 / n_qpairs) return ATTN_ERR_TOO_LARGE;
+  const uintptr_t ormask = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (ormask & 15u) return ATTN_ERR_MISALIGNED;
+  const uint64_t bytes_q = uint64_t(B) * H * Sq * 256, bytes_kv = uint64_t(B) * H * Sk * 256;
+  if (overlaps(out, bytes_q, q, bytes_q) || overlaps(out, bytes_q, k, bytes_kv) ||
+      overlaps(out, bytes_q, v, bytes_kv))
+    return ATTN_ERR_ALIASING;
+
+  // ---- device
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  const int st = device_ready(dev);
+  if (st != ATTN_OK) return st;
+
+  CUtensorMap tq, tk, tv, to;
+  if (!make_map(&tq, q, layout, B, H, Sq, attn::kBM) || !make_map(&tk, k, layout, B, H, Sk, attn::kBN) ||
+      !make_map(&tv, v, layout, B, H, Sk, attn::kBN) || !make_map(&to, out, layout, B, H, Sq, 32))
+    return ATTN_ERR_LAUNCH;
+
+  attn::Params p;
+  p.Sq = static_cast<int>(Sq);
+  p.Sk = static_cast<int>(Sk);
+  p.H = static_cast<int>(H);
+  p.n_qpairs = static_cast<int>(n_qpairs);
+  p.n_kv = static_cast<int>((Sk + attn::kBN - 1) / attn::kBN);
+  p.kv_tail = static_cast<int>(Sk - int64_t(p.n_kv - 1) * attn::kBN);
+  p.layout = layout;
+  p.mode = rounding_mode;
+  p.c = scale * 1.4426950408889634f;
+  p.timeout_ns = kTimeoutNs;
+
+  const unsigned grid = static_cast<unsigned>(B * H * n_qpairs);
+  attn::attn_fwd_kernel<<<grid, attn::kThreads, attn::kSmemBytes,
+                          static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
+}
+
+int attn_fwd_last_error(void) {
+  unsigned int s = 0;
+  if (cudaMemcpyFromSymbol(&s, attn::g_attn_status, sizeof(s)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (s == 0) return ATTN_OK;
+  const unsigned int zero = 0;
+  cudaMemcpyToSymbol(attn::g_attn_status, &zero, sizeof(zero));
+  return ATTN_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,492 @@
+// attn_fwd_kernel.cuh - fused bf16 forward attention for sm_103a (GB300).
+//
+// Computes O = softmax(Q K^T * scale) V for head_dim 128 (snilld.dk,
+// "Open source attention-kernel i HIP slaar AITER v3 paa MI300X", sections
+// "Hvordan kernen arbejder" and "Hvad er udgivet"), rounding the output to bf16
+// per mode (same article, "Numerik samlet eet sted").
+//
+// One CTA owns two 128-row query tiles of one (batch, head) and streams every
+// 128-key tile of K and V through a 4-stage shared-memory ring. Roles (warps):
+//   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ...
+//   warp 1      TMEM allocator and the single tcgen05.mma issuer
+//   warps 4-7   softmax + epilogue of query tile 0 (one TMEM lane = one row)
+//   warps 8-11  softmax + epilogue of query tile 1
+// Tensor memory (512 columns): O0 [0,128), O1 [128,256), S0/P0 [256,384),
+// S1/P1 [384,512). The MMA order per key tile j is
+//   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
+// so the tensor pipe computes one tile's products while the other tile's
+// softmax runs (the pages' "keep the matrix core busy while softmax and loads
+// overlap", section "Hvordan kernen arbejder").
+//
+// Softmax is the online (running-max) form in base 2 with a lazy rescale: O and
+// the row sum are rescaled only when a tile's max exceeds the max in use by more
+// than kTau (log2 units). P is written back into the S columns as two bf16
+// terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi), and O accumulates both
+// products, so the weights carry ~16 significant bits. With P in bf16 alone only
+// ~87% of outputs land within 1 bf16 ULP of the exact result on unit-normal
+// inputs; the two-term P keeps ~99.98% there.
+//
+// Every wait is bounded in time. A wait that expires sets a device status word,
+// raises a CTA-wide abort flag, and every role then stops, waits for its own
+// asynchronous copies and MMAs, frees tensor memory and returns.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kD = 128;                     // head dimension
+constexpr int kBM = 128;                    // query rows per tile
+constexpr int kBN = 128;                    // keys per tile
+constexpr int kQTiles = 2;                  // query tiles per CTA
+constexpr int kStages = 4;                  // K/V ring depth (K and V tiles share it)
+constexpr int kTileBytes = kBM * kD * 2;    // 32 KiB: one 128 x 128 bf16 tile
+constexpr int kHalfBytes = kTileBytes / 2;  // 16 KiB: 128 rows x 64 columns (one TMA box)
+constexpr int kThreads = 384;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kTau = 8.0f;  // lazy-rescale threshold (factor 256)
+
+enum : int {
+  kBarQ = 0,
+  kBarKvFull = 1,
+  kBarKvEmpty = kBarKvFull + kStages,
+  kBarSFull = kBarKvEmpty + kStages,
+  kBarPFull = kBarSFull + kQTiles,
+  kBarOFull = kBarPFull + kQTiles,
+  kBarDrain = kBarOFull + kQTiles,
+  kBarCount = kBarDrain + 1
+};
+
+constexpr int kOffQ = 0;
+constexpr int kOffRing = kOffQ + kQTiles * kTileBytes;
+constexpr int kOffBar = kOffRing + kStages * kTileBytes;
+constexpr int kOffTmemSlot = kOffBar + kBarCount * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+constexpr int kSmemUsed = kOffAbort + 4;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr uint32_t kTmemO0 = 0, kTmemS0 = 256;
+
+struct Params {
+  int Sq, Sk, H;
+  int n_qpairs;  // ceil(Sq / 256)
+  int n_kv;      // ceil(Sk / 128)
+  int kv_tail;   // valid keys in the last key tile, 1..128
+  int layout;    // 0 = BHSD, 1 = BSHD
+  int mode;      // 0 = RTNE, 1 = RTNA, 2 = RTZ
+  float c;       // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+// Bit 0: some wait timed out.
+__device__ unsigned int g_attn_status;
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start,
+// leading and stride byte offsets in 16-byte units, version 1, layout 2).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Waits for `parity` on `bar` for at most timeout_ns. On expiry: sets the abort
+// flag and the device status, returns false. With honor_abort, also returns
+// false as soon as another thread has raised the abort flag.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long timeout_ns, bool honor_abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (ptx::globaltimer() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(&g_attn_status, 1u);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_coords(int layout, int s, int h, int& c1, int& c2) {
+  // BHSD maps are (d, S, H, B); BSHD maps are (d, H, S, B).
+  if (layout == 0) {
+    c1 = s;
+    c2 = h;
+  } else {
+    c1 = h;
+    c2 = s;
+  }
+}
+
+// S = Q K_j^T: 8 MMAs of K = 16 over head_dim; both operands K-major SW128.
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16(kBM, kBN, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    ptx::mma_ss(tmem_d, desc_sw128(q_smem + off, 16, 1024), desc_sw128(k_smem + off, 16, 1024),
+                idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O += P_hi V_j + P_lo V_j. P is in TMEM (A operand); in the 32 columns of key
+// chunk q (keys 32q..32q+31) the first 16 hold P_hi and the next 16 P_lo, two
+// bf16 per column. V_j (keys x head_dim, head_dim contiguous) is the B operand in
+// MN-major SW128: 8-key groups 1024 B apart, the two 64-column halves 16 KiB apart.
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
+                                         bool first) {
+  constexpr uint32_t idesc = idesc_bf16(kBM, kD, 1);
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t a = tmem_p + 32 * (kk >> 1) + 16 * part + 8 * (kk & 1);
+      const uint64_t bd = desc_sw128(v_smem + 2048 * kk, kHalfBytes, 1024);
+      ptx::mma_ts(tmem_o, a, bd, idesc, (first && part == 0 && kk == 0) ? 0u : 1u);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;  // NaN: one pattern
+  if (mode == 0) {
+    u += 0x7FFFu + ((u >> 16) & 1u);  // nearest, ties to even
+  } else if (mode == 1) {
+    u += 0x8000u;  // nearest, ties away from zero (sign-magnitude)
+  }                // mode 2: toward zero = truncate
+  return u >> 16;
+}
+
+// Row extreme of one S tile: max if kPos (scale >= 0), else min (so that
+// scale * extreme is the max of the scaled logits). NaN-propagating. Columns
+// >= valid (key tail) are skipped when kMasked.
+template <bool kMasked, bool kPos>
+__device__ __forceinline__ float tile_extreme(uint32_t tS, int valid) {
+  const float init = kPos ? -__int_as_float(0x7F800000) : __int_as_float(0x7F800000);
+  float e[4] = {init, init, init, init};
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tS + 32 * ch, r);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (kMasked && 32 * ch + i >= valid) continue;
+      const float s = __uint_as_float(r[i]);
+      e[i & 3] = kPos ? ptx::max_nan(e[i & 3], s) : ptx::min_nan(e[i & 3], s);
+    }
+  }
+  if (kPos) return ptx::max_nan(ptx::max_nan(e[0], e[1]), ptx::max_nan(e[2], e[3]));
+  return ptx::min_nan(ptx::min_nan(e[0], e[1]), ptx::min_nan(e[2], e[3]));
+}
+
+// p = 2^(s*c - m_sub); writes P_hi / P_lo over the S columns; returns sum of p.
+template <bool kMasked>
+__device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float m_sub) {
+  const float neg_inf = -__int_as_float(0x7F800000);
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tS + 32 * ch, r);
+    ptx::tmem_wait_ld();
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0 = fmaf(__uint_as_float(r[2 * i]), c, -m_sub);
+      float x1 = fmaf(__uint_as_float(r[2 * i + 1]), c, -m_sub);
+      if (kMasked) {
+        if (32 * ch + 2 * i >= valid) x0 = neg_inf;
+        if (32 * ch + 2 * i + 1 >= valid) x1 = neg_inf;
+      }
+      const float p0 = ptx::ex2(x0);
+      const float p1 = ptx::ex2(x1);
+      l0 += p0;
+      l1 += p1;
+      const uint32_t h = ptx::pack_bf16x2(p0, p1);
+      const float r0 = p0 - __uint_as_float(h << 16);
+      const float r1 = p1 - __uint_as_float(h & 0xFFFF0000u);
+      hi[i] = h;
+      lo[i] = ptx::pack_bf16x2(r0, r1);
+    }
+    ptx::tmem_st16(tS + 32 * ch, hi);
+    ptx::tmem_st16(tS + 32 * ch + 16, lo);
+  }
+  return l0 + l1;
+}
+
+__device__ __forceinline__ void scale_o(uint32_t tO, float f) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tO + 32 * ch, r);
+    ptx::tmem_wait_ld();
+    uint32_t a[16], b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      a[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+      b[i] = __float_as_uint(__uint_as_float(r[16 + i]) * f);
+    }
+    ptx::tmem_st16(tO + 32 * ch, a);
+    ptx::tmem_st16(tO + 32 * ch + 16, b);
+  }
+  ptx::tmem_wait_st();
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long timeout_ns) {
+  const bool ok = wait_bounded(bar, parity, abort_flag, timeout_ns, true);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  const uint32_t sQ = sbase + kOffQ;
+  const uint32_t sRing = sbase + kOffRing;
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x % p.n_qpairs;
+  const int bh = blockIdx.x / p.n_qpairs;
+  const int head = bh % p.H;
+  const int batch = bh / p.H;
+  const int n_kv = p.n_kv;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(kBarKvFull + s), 1);
+      ptx::mbar_init(bar(kBarKvEmpty + s), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      ptx::mbar_init(bar(kBarSFull + t), 1);
+      ptx::mbar_init(bar(kBarPFull + t), 128);
+      ptx::mbar_init(bar(kBarOFull + t), 1);
+    }
+    ptx::mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+    ptx::prefetch_tmap(&tm_o);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int fills[kStages] = {0, 0, 0, 0};
+      bool ok = true;
+      int c1, c2;
+      ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
+      for (int t = 0; t < kQTiles; ++t) {
+        tma_coords(p.layout, (2 * pair + t) * kBM, head, c1, c2);
+        for (int hf = 0; hf < 2; ++hf)
+          ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
+                           batch);
+      }
+      for (int it = 0; it < 2 * n_kv; ++it) {
+        const int stage = it % kStages;
+        const uint32_t parity = ((it / kStages) & 1) ^ 1;
+        if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) {
+          ok = false;
+          break;
+        }
+        const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+        tma_coords(p.layout, (it >> 1) * kBN, head, c1, c2);
+        ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
+                           64 * hf, c1, c2, batch);
+        ++fills[stage];
+      }
+      if (!ok) {
+        // Abort: let every copy this thread started land before the CTA exits.
+        wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
+        for (int s = 0; s < kStages; ++s)
+          if (fills[s] > 0)
+            wait_bounded(bar(kBarKvFull + s), (fills[s] - 1) & 1, abort_flag, p.timeout_ns, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
+      ptx::tc_fence_after();
+      auto ring_wait = [&](int it) -> bool {
+        const bool r = wait_bounded(bar(kBarKvFull + it % kStages), (it / kStages) & 1, abort_flag,
+                                    p.timeout_ns, true);
+        ptx::tc_fence_after();
+        return r;
+      };
+      auto ring_addr = [&](int it) -> uint32_t { return sRing + (it % kStages) * kTileBytes; };
+      if (ok) ok = ring_wait(0);
+      if (ok) {
+        issue_s(tmem + kTmemS0, sQ, ring_addr(0));
+        ptx::mma_commit(bar(kBarSFull + 0));
+        issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(0));
+        ptx::mma_commit(bar(kBarSFull + 1));
+        ptx::mma_commit(bar(kBarKvEmpty + 0));
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int vit = 2 * j + 1;
+        const int kit = 2 * j + 2;
+        const bool more = j + 1 < n_kv;
+        if (!(ok = ring_wait(vit))) break;
+        if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
+        ptx::tc_fence_after();
+        issue_pv(tmem + kTmemO0, tmem + kTmemS0, ring_addr(vit), j == 0);
+        if (!more) ptx::mma_commit(bar(kBarOFull + 0));
+        if (more) {
+          if (!(ok = ring_wait(kit))) break;
+          issue_s(tmem + kTmemS0, sQ, ring_addr(kit));
+          ptx::mma_commit(bar(kBarSFull + 0));
+        }
+        if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
+        ptx::tc_fence_after();
+        issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, ring_addr(vit), j == 0);
+        ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
+        if (!more) ptx::mma_commit(bar(kBarOFull + 1));
+        if (more) {
+          issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(kit));
+          ptx::mma_commit(bar(kBarSFull + 1));
+          ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+        }
+      }
+      if (!ok) {
+        // Abort: wait until every MMA issued so far has finished.
+        ptx::mma_commit(bar(kBarDrain));
+        wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kSoftmaxWarp0) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int t = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;                    // TMEM lane quarter of this warp
+    const int row = wq * 32 + lane;             // row within the query tile
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kTmemS0 + 128 * t;
+    const uint32_t tO = tmem + lane_base + kTmemO0 + 128 * t;
+    const float c = p.c;
+    const bool pos = c >= 0.f;
+    const float neg_inf = -__int_as_float(0x7F800000);
+    float m_used = neg_inf;
+    float l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n_kv; ++j) {
+      if (!(ok = warp_wait(bar(kBarSFull + t), j & 1, abort_flag, p.timeout_ns))) break;
+      ptx::tc_fence_after();
+      const bool last = (j == n_kv - 1) && (p.kv_tail < kBN);
+      float ext;
+      if (last) {
+        ext = pos ? tile_extreme<true, true>(tS, p.kv_tail) : tile_extreme<true, false>(tS, p.kv_tail);
+      } else {
+        ext = pos ? tile_extreme<false, true>(tS, kBN) : tile_extreme<false, false>(tS, kBN);
+      }
+      const float m_tile = ext * c;
+      const bool need = m_tile > m_used + kTau;  // false for NaN
+      if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
+        // O holds every product up to key tile j-1 and nothing newer: the MMA
+        // that wrote S_j was issued after PV_{j-1}, and PV_j waits for P_j.
+        scale_o(tO, need ? ptx::ex2(m_used - m_tile) : 1.0f);
+      }
+      if (need) {
+        l *= ptx::ex2(m_used - m_tile);
+        m_used = m_tile;
+      }
+      const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
+      l += last ? tile_exp<true>(tS, p.kv_tail, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kBarPFull + t));
+    }
+
+    if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
+    if (ok) {
+      ptx::tc_fence_after();
+      // Normalise, round, stage in the (now free) Q tile buffer with the TMA
+      // 128-byte swizzle, and store this warp's 32 rows with two TMA boxes.
+      const uint32_t stage_base = sQ + t * kTileBytes;
+      const int mode = p.mode;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tO + 32 * ch, r);
+        ptx::tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float o0 = __fdiv_rn(__uint_as_float(r[2 * i]), l);
+          const float o1 = __fdiv_rn(__uint_as_float(r[2 * i + 1]), l);
+          w[i] = round_bf16_bits(o0, mode) | (round_bf16_bits(o1, mode) << 16);
+        }
+        const uint32_t half_base = stage_base + (ch >> 1) * kHalfBytes + row * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = (ch & 1) * 4 + u;
+          ptx::st_shared_v4(half_base + ((chunk ^ (row & 7)) << 4), w[4 * u], w[4 * u + 1],
+                            w[4 * u + 2], w[4 * u + 3]);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int q_row0 = (2 * pair + t) * kBM + wq * 32;
+        if (q_row0 < p.Sq) {
+          int c1, c2;
+          tma_coords(p.layout, q_row0, head, c1, c2);
+          for (int hf = 0; hf < 2; ++hf)
+            ptx::tma_store_4d(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1, c2,
+                              batch);
+          ptx::bulk_commit_group();
+          ptx::bulk_wait_group_0();
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace attn

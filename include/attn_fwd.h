@@ -1,0 +1,101 @@
+/*
+ * attn_fwd.h - C ABI of the GB300 (sm_103a) bf16 forward-attention library.
+ *
+ * The operation is the fused forward attention described on the pages about
+ * MoonMath AI's bf16 attention kernel:
+ *   - snilld.dk, "Open source attention-kernel i HIP slaar AITER v3 paa MI300X -
+ *     hurtigere bf16-attention uden assembly":
+ *       "Hvordan kernen arbejder": O = softmax(Q K^T / sqrt(d)) V in one fused
+ *         pass, bf16 output;
+ *       "Hvad er udgivet": BSHD and BHSD inputs read without a transpose,
+ *         head_dim 128, arbitrary sequence lengths, cross-attention (Sq != Sk);
+ *       "Numerik samlet eet sted": output rounded to bf16 per mode, finite
+ *         values within 1 bf16 ULP, NaN/Inf bit-identical, deterministic.
+ *   - tilnote.io note on the same kernel, performance section: the modes are
+ *     RTNE, RTNA and RTZ; no causal mask, no GQA, no varlen batching.
+ *
+ * Every entry point is a plain C function. Pointers marked "device" must point
+ * to memory of the current CUDA device; the library never copies them to the
+ * host, never frees them and keeps no reference after the call returns.
+ */
+#ifndef ATTN_FWD_H
+#define ATTN_FWD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Tensor layouts. Q, K, V and O all use the one layout given to the call.
+ *   BHSD: element (b, h, s, c) at ((b*H + h)*S + s)*128 + c
+ *   BSHD: element (b, h, s, c) at ((b*S + s)*H + h)*128 + c
+ * with S = Sq for Q and O, S = Sk for K and V. Tensors are contiguous. */
+typedef enum { ATTN_LAYOUT_BHSD = 0, ATTN_LAYOUT_BSHD = 1 } attn_layout_t;
+
+/* bf16 rounding of the output (from the fp32 accumulator):
+ *   RTNE nearest, ties to even; RTNA nearest, ties away from zero;
+ *   RTZ toward zero. NaN outputs are written as 0x7FC0; signed zeros and
+ *   bf16 subnormals are kept. */
+typedef enum { ATTN_ROUND_RTNE = 0, ATTN_ROUND_RTNA = 1, ATTN_ROUND_RTZ = 2 } attn_round_t;
+
+/* Status codes. Errors other than ATTN_ERR_LAUNCH and ATTN_ERR_TIMEOUT are
+ * found on the host before anything is launched. */
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1, /* null pointer, a size < 1, non-finite scale     */
+  ATTN_ERR_UNSUPPORTED = -2, /* d != 128, unknown layout or rounding mode      */
+  ATTN_ERR_MISALIGNED = -3,  /* a pointer not 16-byte aligned                  */
+  ATTN_ERR_ALIASING = -4,    /* out overlaps q, k or v                         */
+  ATTN_ERR_NO_DEVICE = -5,   /* no current CUDA device                         */
+  ATTN_ERR_ARCH = -6,        /* current device is not compute capability 10.3  */
+  ATTN_ERR_LAUNCH = -7,      /* the CUDA launch (or tensor-map setup) failed   */
+  ATTN_ERR_TIMEOUT = -8,     /* a bounded device-side wait expired             */
+  ATTN_ERR_TOO_LARGE = -9    /* a size beyond the tensor-map / grid limits     */
+};
+
+/*
+ * attn_fwd - O = softmax(Q K^T * scale) V for every (b, h).
+ *
+ *   q    device, bf16, B*H*Sq*d elements in `layout`      (read only)
+ *   k    device, bf16, B*H*Sk*d elements in `layout`      (read only)
+ *   v    device, bf16, B*H*Sk*d elements in `layout`      (read only)
+ *   out  device, bf16, B*H*Sq*d elements in `layout`      (written; must not
+ *        overlap q, k or v)
+ *   layout         ATTN_LAYOUT_BHSD or ATTN_LAYOUT_BSHD
+ *   B, H, Sq, Sk   batch, heads, query length, key length; each >= 1, Sq and
+ *                  Sk need not be multiples of anything and may differ
+ *   d              head dimension; must be 128
+ *   scale          logit scale, any finite float (1/sqrt(128) in the pages)
+ *   rounding_mode  ATTN_ROUND_RTNE, ATTN_ROUND_RTNA or ATTN_ROUND_RTZ
+ *   stream         cudaStream_t to run on (NULL = legacy default stream)
+ *
+ * Asynchronous: returns after the launch; `out` is valid once the stream has
+ * reached the call. All pointers must be 16-byte aligned. The call allocates
+ * no device memory. Results are bit-identical from run to run. Thread-safe.
+ * Returns ATTN_OK or a negative status code.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
+             int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+             int rounding_mode, void* stream);
+
+/* Static English text for a status code (never NULL). */
+const char* attn_status_str(int status);
+
+/*
+ * Device-side status of earlier launches on the current device: ATTN_OK, or
+ * ATTN_ERR_TIMEOUT if some launch gave up on a wait that did not finish within
+ * its time limit (the kernel then stops its work, waits for its own copies in
+ * flight, frees its tensor memory and returns; its output is undefined).
+ * Reading clears the status. Synchronize the stream that ran the calls first.
+ */
+int attn_fwd_last_error(void);
+
+/* Library version, as MAJOR*10000 + MINOR*100 + PATCH. */
+int attn_fwd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H */

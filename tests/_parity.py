@@ -1,0 +1,55 @@
+"""Comparison of CUDA output against the fp64 oracle (test helper).
+
+The bar (from the numerics contract of the attention pages: snilld.dk article,
+section "Numerik samlet eet sted", re-targeted at the exact fp64 result):
+  * every NaN / +-Inf position and bit pattern matches exactly;
+  * at least 99.9% of finite elements are within 1 bf16 ULP of the oracle's
+    rounding (same mode) of the exact value;
+  * max |err| against the exact fp64 value <= 8e-3 for unit-normal inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import bf16_bits_to_f64, nonfinite_bits, round_bf16, ulp_distance
+
+ULP_FRACTION = 0.999
+MAX_ABS_ERR = 8e-3
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor (any device) -> uint16 numpy array of its bit patterns."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f64_of(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def compare(gpu_bits: np.ndarray, exact: np.ndarray, mode: str) -> dict:
+    want = round_bf16(exact, mode)
+    nf_w = nonfinite_bits(want)
+    nf_g = nonfinite_bits(gpu_bits)
+    fin = ~nf_w
+    d = ulp_distance(gpu_bits[fin], want[fin]) if fin.any() else np.zeros(0, np.int64)
+    g = bf16_bits_to_f64(gpu_bits[fin])
+    err = np.abs(g - exact[fin]) if fin.any() else np.zeros(0)
+    return {
+        "n": int(gpu_bits.size),
+        "n_nonfinite": int(nf_w.sum()),
+        "nonfinite_positions_match": bool((nf_w == nf_g).all()),
+        "nonfinite_bits_match": bool((gpu_bits[nf_w] == want[nf_w]).all()),
+        "within_1ulp": float((d <= 1).mean()) if d.size else 1.0,
+        "max_ulp": int(d.max()) if d.size else 0,
+        "max_abs_err": float(err.max()) if err.size else 0.0,
+        "exact_match": float((d == 0).mean()) if d.size else 1.0,
+    }
+
+
+def assert_parity(stats: dict, max_abs_err: float | None = MAX_ABS_ERR):
+    assert stats["nonfinite_positions_match"], stats
+    assert stats["nonfinite_bits_match"], stats
+    assert stats["within_1ulp"] >= ULP_FRACTION, stats
+    if max_abs_err is not None:
+        assert stats["max_abs_err"] <= max_abs_err, stats

@@ -1,0 +1,106 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+import torch
+
+import bf16_forward_attention_gb300 as attn
+from bf16_forward_attention_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_fwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not build.up_to_date():
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("library not built and nvcc not available")
+        build.build()
+    return attn.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_entry_points():
+    names = _declared_functions()
+    assert {"attn_fwd", "attn_status_str", "attn_fwd_last_error", "attn_fwd_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in range(0, -10, -1):
+        s = attn.status_str(st)
+        assert s and s != "unknown status", st
+    assert attn.status_str(-1234) == "unknown status"
+    assert lib.attn_fwd_version() >= 100
+
+
+A = 1 << 20  # fake, 16-byte aligned addresses: never dereferenced on these paths
+
+
+def _call(q=A, k=2 * A, v=3 * A, o=4 * A, layout=0, B=1, H=2, Sq=256, Sk=256, d=128,
+          scale=0.088, mode=0):
+    return attn.attn_fwd_raw(q, k, v, o, layout, B, H, Sq, Sk, d, scale, mode, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(H=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Sk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(layout=2), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(mode=3), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(mode=-1), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(o=4 * A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(o=A), attn.ATTN_ERR_ALIASING),
+    (dict(o=3 * A + 4096), attn.ATTN_ERR_ALIASING),
+    (dict(Sq=1 << 31), attn.ATTN_ERR_TOO_LARGE),
+    (dict(H=1 << 20, Sq=1 << 20, Sk=1 << 20), attn.ATTN_ERR_TOO_LARGE),
+])
+def test_host_validation(lib, kw, status):
+    assert _call(**kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
+def test_valid_call_without_gpu_reports_no_device(lib):
+    assert _call() == attn.ATTN_ERR_NO_DEVICE
+
+
+def test_python_binding_checks(lib):
+    x = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        attn.attn_fwd(x, x, x)  # CPU tensors are refused before any call
+    with pytest.raises(ValueError):
+        attn.attn_fwd(x, x, x, layout="sbhd")
+    with pytest.raises(ValueError):
+        attn.attn_fwd(x, x, x, rounding="rtp")
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "bf16_forward_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
+                assert "oracle/" not in src, f
