@@ -1,0 +1,344 @@
+"""Benchmark: bf16 forward attention on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload self8k|cross4k32k|long128k|stress16381|tiny]
+
+Workload (default): self-attention, BSHD, B=2, H=16, Sq=Sk=8192, d=128, bf16
+Q/K/V ~ N(0,1) from a fixed seed, scale 1/sqrt(128). One step = one call of the
+fused kernel per output rounding mode (RTNE, RTNA, RTZ) over the same inputs.
+Metric: TFLOP/s counted as 4*B*H*Sq*Sk*d per call, and the fraction of the
+measured dense bf16 peak. Inputs (192 MiB) exceed the 129 MB L2; L2 is not
+flushed between steps.
+
+--impl reference times the fp64 CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload, in the same unit.
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own GPU
+(weak scaling, no data exchange); rank 0 prints the max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# Pin the BLAS thread count before numpy loads, so the CPU baseline states the
+# number of threads it actually used.
+_CPU_THREADS = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CPU_THREADS))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CPU_THREADS))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (4·B·H·Sq·Sk·d) and % of GB300 dense bf16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_BYTES = 129e6
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons every 200 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                stamp, frac = (parts[0].split(".") + ["0"])[:2]
+                ts = time.mktime(time.strptime(stamp, "%Y/%m/%d %H:%M:%S")) + float("0." + frac)
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        reasons = sorted({n for r in use for n, v in zip(self.REASONS, r[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole run (timed region shorter than a sample)"}
+
+
+def _cpu_sample(w, q, k, v, budget_s: float):
+    """The oracle on host cores: whole row blocks of successive heads until the
+    time budget is used. Returns (flops counted, seconds, rows)."""
+    from oracle import attention_rows_fp64, bf16_bits_to_f64, to_bhsd
+    from bf16_forward_attention_gb300 import inputs
+
+    qb, kb, vb = (to_bhsd(t.view(torch.int16).numpy(), w.layout) for t in (q, k, v))
+    scale = inputs.default_scale()
+    rows_done, t_used, i = 0, 0.0, 0
+    block = 256
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    while t_used < budget_s:
+        b, h = heads[i % len(heads)]
+        r0 = ((i // len(heads)) * block) % w.Sq
+        rows = np.arange(r0, min(w.Sq, r0 + block))
+        kh, vh, qh = bf16_bits_to_f64(kb[b, h]), bf16_bits_to_f64(vb[b, h]), bf16_bits_to_f64(qb[b, h])
+        t0 = time.perf_counter()
+        attention_rows_fp64(qh, kh, vh, scale, rows)
+        t_used += time.perf_counter() - t0
+        rows_done += rows.size
+        i += 1
+    return 4.0 * rows_done * w.Sk * w.D, t_used, rows_done
+
+
+def _config(w, world):
+    big = 3 * 2 * w.B * w.H * max(w.Sq, w.Sk) * w.D > L2_BYTES
+    return {"workload": f"{w.name}: {'self' if w.Sq == w.Sk else 'cross'}-attention fwd, "
+                        f"{w.layout.upper()}, B={w.B}, H={w.H}, Sq={w.Sq}, Sk={w.Sk}, d={w.D}, "
+                        f"rounding {'/'.join(m.upper() for m in w.roundings)}",
+            "layout": w.layout, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.D,
+            "roundings": list(w.roundings), "calls_per_step": len(w.roundings),
+            "qk_dist": f"N(0,{w.qk_std:g}^2)", "v_dist": "N(0,1)" if w.v_dist == "normal" else "U(-1,1)",
+            "specials": w.specials, "seed": w.seed,
+            "l2": "inputs larger than L2 (not flushed)" if big else "inputs fit in L2 (not flushed)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from bf16_forward_attention_gb300 import inputs
+
+    q, k, v = inputs.make_qkv(w)
+    done = []
+    for i in range(args.warmup + args.steps):
+        f, t, rows = _cpu_sample(w, q, k, v, budget_s=args.ref_step_seconds)
+        if i >= args.warmup:
+            done.append((f, t, rows))
+    t_total = sum(t for _, t, _ in done)
+    value = sum(f for f, _, _ in done) / t_total / 1e12
+    rows = sum(r for _, _, r in done)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / max(1, len(done)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
+                         "sample": f"{rows} query rows of the workload, each against all {w.Sk} keys "
+                                   f"(~{args.ref_step_seconds:g} s of fp64 CPU work per step)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    world, rank, local = _dist()
+    import bf16_forward_attention_gb300 as attn
+    from bf16_forward_attention_gb300 import inputs
+
+    attn.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    q_h, k_h, v_h = inputs.make_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    outs = {m: torch.empty_like(q) for m in w.roundings}
+    stream = torch.cuda.current_stream(dev)
+    flops_call = float(w.flops)
+
+    def step():
+        for m in w.roundings:
+            attn.attn_fwd(q, k, v, layout=w.layout, rounding=m, out=outs[m])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if attn.attn_fwd_last_error() != attn.ATTN_OK:
+        raise RuntimeError("a device-side wait timed out during warm-up")
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.6)  # nvidia-smi takes a moment to start sampling
+    n_calls = args.steps * len(w.roundings)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_calls)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark("t0")
+    t_start.record(stream)
+    i = 0
+    for _ in range(args.steps):
+        for m in w.roundings:
+            ev[i][0].record(stream)
+            attn.attn_fwd(q, k, v, layout=w.layout, rounding=m, out=outs[m])
+            ev[i][1].record(stream)
+            i += 1
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t1")
+    if dist:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
+    clocks = sampler.stop() if rank == 0 else None
+    if attn.attn_fwd_last_error() != attn.ATTN_OK:
+        raise RuntimeError("a device-side wait timed out in the timed region")
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    # End to end through the public API: pinned host inputs -> device -> one call
+    # per mode -> results back to pinned host memory, all inside the timed region.
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    host_out = {m: torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory() for m in w.roundings}
+
+    def e2e_step():
+        qd, kd, vd = (t.to(dev, non_blocking=True) for t in (qp, kp, vp))
+        for m in w.roundings:
+            host_out[m].copy_(attn.attn_fwd(qd, kd, vd, layout=w.layout, rounding=m),
+                              non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(3, min(10, args.steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / e_steps
+    e2e = {"value": flops_call * len(w.roundings) / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "ms_per_step": e_ms,
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h)),
+           "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values())}
+
+    peaks, peak_src = _peaks()
+    timed_s = elapsed_ms * 1e-3
+    sustained = timed_s >= 1.0
+    peak = float(peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    achieved = flops_call / (avg_launch_ms * 1e-3) / 1e12
+    value = world * flops_call * n_calls / timed_s / 1e12
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        f, t, rows = _cpu_sample(w, q_h, k_h, v_h, budget_s=args.cpu_seconds)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
+               "sample": f"{rows} query rows of the workload, each against all {w.Sk} keys "
+                         f"({t:.1f} s of fp64 CPU work)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": _config(w, world),
+        "pct_of_dense_bf16_peak": 100.0 * achieved / peak,
+        "launch_ms": {"median": launch_ms[len(launch_ms) // 2],
+                      "p5": launch_ms[int(0.05 * (len(launch_ms) - 1))],
+                      "p95": launch_ms[int(0.95 * (len(launch_ms) - 1))], "n": len(launch_ms)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": args.traffic,
+                     "peak_kind": f"{'sustained' if sustained else 'burst'} dense bf16 ({peak_src})",
+                     "kernel": "attn_fwd_kernel",
+                     "note": "achieved counts 4*B*H*Sq*Sk*d per launch; the kernel also runs the "
+                             "P_lo*V product, 1.5x the counted tensor work"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": n_calls,
+        "clocks": clocks,
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="self8k")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the kernel, from an ncu capture")
+    args = ap.parse_args()
+    if args.impl == "ours" and args.warmup < 3:
+        args.warmup = 3
+    from bf16_forward_attention_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -60,6 +60,19 @@ int device_ready(int dev) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
   }
+  // The kernel's warpgroups re-split the registers a CTA is launched with
+  // (setmaxnreg); the split only adds up if each thread starts with exactly
+  // kLaunchRegs. A build with another count would make setmaxnreg.inc wait
+  // forever, so it is refused here.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, attn::attn_fwd_kernel) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  if (fa.numRegs != attn::kLaunchRegs) {
+    g_dev_state[dev] = ATTN_ERR_LAUNCH;
+    return ATTN_ERR_LAUNCH;
+  }
   g_dev_state[dev] = 1;
   return ATTN_OK;
 }

@@ -9,8 +9,12 @@
 // 128-key tile of K and V through a 4-stage shared-memory ring. Roles (warps):
 //   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ...
 //   warp 1      TMEM allocator and the single tcgen05.mma issuer
+//   warps 2-3   idle (they complete the first warpgroup)
 //   warps 4-7   softmax + epilogue of query tile 0 (one TMEM lane = one row)
 //   warps 8-11  softmax + epilogue of query tile 1
+// The launch gives every thread 168 registers; the first warpgroup hands most of
+// its share to the two softmax warpgroups (56 + 2 * 224 = 3 * 168), which each
+// keep a 128-float output row per thread.
 // Tensor memory (512 columns): O0 [0,128), O1 [128,256), S0/P0 [256,384),
 // S1/P1 [384,512). The MMA order per key tile j is
 //   PV0_j, S0_{j+1}, PV1_j, S1_{j+1}
@@ -18,13 +22,19 @@
 // softmax runs (the pages' "keep the matrix core busy while softmax and loads
 // overlap", section "Hvordan kernen arbejder").
 //
-// Softmax is the online (running-max) form in base 2 with a lazy rescale: O and
-// the row sum are rescaled only when a tile's max exceeds the max in use by more
-// than kTau (log2 units). P is written back into the S columns as two bf16
-// terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi), and O accumulates both
-// products, so the weights carry ~16 significant bits. With P in bf16 alone only
-// ~87% of outputs land within 1 bf16 ULP of the exact result on unit-normal
-// inputs; the two-term P keeps ~99.98% there.
+// Softmax is the online (running-max) form in base 2 with a lazy rescale: the
+// running output and row sum are rescaled only when a tile's max exceeds the max
+// in use by more than kTau (log2 units). P is written back into the S columns as
+// two bf16 terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi), and both products
+// are accumulated, so the weights carry ~16 significant bits. With P in bf16
+// alone only ~87% of outputs land within 1 bf16 ULP of the exact result on
+// unit-normal inputs; the two-term P keeps ~99.98% there.
+//
+// The tensor pipe's fp32 accumulation truncates; summed over tens of thousands
+// of keys that bias costs ~0.3% (32K keys) to ~1.5% (128K keys) of outputs their
+// 1-ULP bound. So the PV products of each key tile go into a fresh TMEM
+// accumulator (16 MMAs deep), and each softmax thread adds it into its row's 128
+// fp32 registers, rounding to nearest, before it hands over the next P.
 //
 // Every wait is bounded in time. A wait that expires sets a device status word,
 // raises a CTA-wide abort flag, and every role then stops, waits for its own
@@ -46,6 +56,10 @@ constexpr int kTileBytes = kBM * kD * 2;    // 32 KiB: one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;  // 16 KiB: 128 rows x 64 columns (one TMA box)
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;
+constexpr int kLaunchRegs = 168;     // per thread at launch: 65536 / 384, rounded to 8
+constexpr uint32_t kRegsLow = 56;    // producer / MMA warpgroup after the split
+constexpr uint32_t kRegsHigh = 224;  // each softmax warpgroup after the split
+static_assert(kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (factor 256)
 
@@ -103,7 +117,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
 // Waits for `parity` on `bar` for at most timeout_ns. On expiry: sets the abort
 // flag and the device status, returns false. With honor_abort, also returns
 // false as soon as another thread has raised the abort flag.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned long long timeout_ns, bool honor_abort) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -132,7 +146,7 @@ __device__ __forceinline__ void tma_coords(int layout, int s, int h, int& c1, in
 // S = Q K_j^T: 8 MMAs of K = 16 over head_dim; both operands K-major SW128.
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t idesc = idesc_bf16(kBM, kBN, 0);
-#pragma unroll
+#pragma unroll 1
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
     ptx::mma_ss(tmem_d, desc_sw128(q_smem + off, 16, 1024), desc_sw128(k_smem + off, 16, 1024),
@@ -140,21 +154,18 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32
   }
 }
 
-// O += P_hi V_j + P_lo V_j. P is in TMEM (A operand); in the 32 columns of key
-// chunk q (keys 32q..32q+31) the first 16 hold P_hi and the next 16 P_lo, two
-// bf16 per column. V_j (keys x head_dim, head_dim contiguous) is the B operand in
-// MN-major SW128: 8-key groups 1024 B apart, the two 64-column halves 16 KiB apart.
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
-                                         bool first) {
+// O_j = P_hi V_j + P_lo V_j into a fresh accumulator. P is in TMEM (A operand):
+// the 16 columns of key chunk u (keys 16u..16u+15) hold P_hi in their first 8
+// and P_lo in their last 8 columns, two bf16 per column. V_j (keys x head_dim,
+// head_dim contiguous) is the B operand in MN-major SW128: 8-key groups 1024 B
+// apart, the two 64-column halves 16 KiB apart.
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem) {
   constexpr uint32_t idesc = idesc_bf16(kBM, kD, 1);
-#pragma unroll
-  for (int part = 0; part < 2; ++part) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t a = tmem_p + 32 * (kk >> 1) + 16 * part + 8 * (kk & 1);
-      const uint64_t bd = desc_sw128(v_smem + 2048 * kk, kHalfBytes, 1024);
-      ptx::mma_ts(tmem_o, a, bd, idesc, (first && part == 0 && kk == 0) ? 0u : 1u);
-    }
+#pragma unroll 1
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t bd = desc_sw128(v_smem + 2048 * kk, kHalfBytes, 1024);
+    ptx::mma_ts(tmem_o, tmem_p + 16 * kk, bd, idesc, kk == 0 ? 0u : 1u);
+    ptx::mma_ts(tmem_o, tmem_p + 16 * kk + 8, bd, idesc, 1u);
   }
 }
 
@@ -176,11 +187,10 @@ template <bool kMasked, bool kPos>
 __device__ __forceinline__ float tile_extreme(uint32_t tS, int valid) {
   const float init = kPos ? -__int_as_float(0x7F800000) : __int_as_float(0x7F800000);
   float e[4] = {init, init, init, init};
-#pragma unroll
+#pragma unroll 1
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t r[32];
     ptx::tmem_ld32(tS + 32 * ch, r);
-    ptx::tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (kMasked && 32 * ch + i >= valid) continue;
@@ -192,24 +202,24 @@ __device__ __forceinline__ float tile_extreme(uint32_t tS, int valid) {
   return ptx::min_nan(ptx::min_nan(e[0], e[1]), ptx::min_nan(e[2], e[3]));
 }
 
-// p = 2^(s*c - m_sub); writes P_hi / P_lo over the S columns; returns sum of p.
+// p = 2^(s*c - m_sub); writes P_hi / P_lo over the S columns (16-key chunks:
+// 8 columns of P_hi then 8 of P_lo); returns the sum of p.
 template <bool kMasked>
 __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float m_sub) {
   const float neg_inf = -__int_as_float(0x7F800000);
   float l0 = 0.f, l1 = 0.f;
+#pragma unroll 1
+  for (int u = 0; u < 8; ++u) {
+    uint32_t r[16];
+    ptx::tmem_ld16(tS + 16 * u, r);
+    uint32_t hi[8], lo[8];
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    uint32_t r[32];
-    ptx::tmem_ld32(tS + 32 * ch, r);
-    ptx::tmem_wait_ld();
-    uint32_t hi[16], lo[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       float x0 = fmaf(__uint_as_float(r[2 * i]), c, -m_sub);
       float x1 = fmaf(__uint_as_float(r[2 * i + 1]), c, -m_sub);
       if (kMasked) {
-        if (32 * ch + 2 * i >= valid) x0 = neg_inf;
-        if (32 * ch + 2 * i + 1 >= valid) x1 = neg_inf;
+        if (16 * u + 2 * i >= valid) x0 = neg_inf;
+        if (16 * u + 2 * i + 1 >= valid) x1 = neg_inf;
       }
       const float p0 = ptx::ex2(x0);
       const float p1 = ptx::ex2(x1);
@@ -221,28 +231,25 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float
       hi[i] = h;
       lo[i] = ptx::pack_bf16x2(r0, r1);
     }
-    ptx::tmem_st16(tS + 32 * ch, hi);
-    ptx::tmem_st16(tS + 32 * ch + 16, lo);
+    ptx::tmem_st8(tS + 16 * u, hi);
+    ptx::tmem_st8(tS + 16 * u + 8, lo);
   }
   return l0 + l1;
 }
 
-__device__ __forceinline__ void scale_o(uint32_t tO, float f) {
+// acc += O (the finished key tile's products), then acc *= f when rescaling.
+__device__ __forceinline__ void fold_tile(uint32_t tO, float (&acc)[kD], bool rescale, float f) {
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t r[32];
     ptx::tmem_ld32(tO + 32 * ch, r);
-    ptx::tmem_wait_ld();
-    uint32_t a[16], b[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      a[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-      b[i] = __float_as_uint(__uint_as_float(r[16 + i]) * f);
-    }
-    ptx::tmem_st16(tO + 32 * ch, a);
-    ptx::tmem_st16(tO + 32 * ch + 16, b);
+    for (int i = 0; i < 32; ++i) acc[32 * ch + i] += __uint_as_float(r[i]);
   }
-  ptx::tmem_wait_st();
+  if (rescale) {
+#pragma unroll
+    for (int i = 0; i < kD; ++i) acc[i] *= f;
+  }
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -304,96 +311,103 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int fills[kStages] = {0, 0, 0, 0};
-      bool ok = true;
-      int c1, c2;
-      ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
-      for (int t = 0; t < kQTiles; ++t) {
-        tma_coords(p.layout, (2 * pair + t) * kBM, head, c1, c2);
-        for (int hf = 0; hf < 2; ++hf)
-          ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
-                           batch);
-      }
-      for (int it = 0; it < 2 * n_kv; ++it) {
-        const int stage = it % kStages;
-        const uint32_t parity = ((it / kStages) & 1) ^ 1;
-        if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) {
-          ok = false;
-          break;
+  // Each role changes its register budget inside its own branch, so that the
+  // budget of every instruction is known where it is compiled.
+  if (warp < kSoftmaxWarp0) {
+    ptx::setmaxnreg_dec<kRegsLow>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
+        bool ok = true;
+        int c1, c2;
+        ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
+        for (int t = 0; t < kQTiles; ++t) {
+          tma_coords(p.layout, (2 * pair + t) * kBM, head, c1, c2);
+          for (int hf = 0; hf < 2; ++hf)
+            ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
+                             batch);
         }
-        const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-        tma_coords(p.layout, (it >> 1) * kBN, head, c1, c2);
-        ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
-        for (int hf = 0; hf < 2; ++hf)
-          ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
-                           64 * hf, c1, c2, batch);
-        ++fills[stage];
+        for (int it = 0; it < 2 * n_kv; ++it) {
+          const int stage = it % kStages;
+          const uint32_t parity = ((it / kStages) & 1) ^ 1;
+          if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+          tma_coords(p.layout, (it >> 1) * kBN, head, c1, c2);
+          ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
+          for (int hf = 0; hf < 2; ++hf)
+            ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
+                             64 * hf, c1, c2, batch);
+          ++issued;
+        }
+        if (!ok) {
+          // Abort: let every copy this thread started land before the CTA exits.
+          wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
+          for (int s = 0; s < kStages && s < issued; ++s) {
+            const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
+            wait_bounded(bar(kBarKvFull + s), (fills - 1) & 1, abort_flag, p.timeout_ns, false);
+          }
+        }
       }
-      if (!ok) {
-        // Abort: let every copy this thread started land before the CTA exits.
-        wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
-        for (int s = 0; s < kStages; ++s)
-          if (fills[s] > 0)
-            wait_bounded(bar(kBarKvFull + s), (fills[s] - 1) & 1, abort_flag, p.timeout_ns, false);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
-      ptx::tc_fence_after();
-      auto ring_wait = [&](int it) -> bool {
-        const bool r = wait_bounded(bar(kBarKvFull + it % kStages), (it / kStages) & 1, abort_flag,
-                                    p.timeout_ns, true);
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
         ptx::tc_fence_after();
-        return r;
-      };
-      auto ring_addr = [&](int it) -> uint32_t { return sRing + (it % kStages) * kTileBytes; };
-      if (ok) ok = ring_wait(0);
-      if (ok) {
-        issue_s(tmem + kTmemS0, sQ, ring_addr(0));
-        ptx::mma_commit(bar(kBarSFull + 0));
-        issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(0));
-        ptx::mma_commit(bar(kBarSFull + 1));
-        ptx::mma_commit(bar(kBarKvEmpty + 0));
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int vit = 2 * j + 1;
-        const int kit = 2 * j + 2;
-        const bool more = j + 1 < n_kv;
-        if (!(ok = ring_wait(vit))) break;
-        if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
-        ptx::tc_fence_after();
-        issue_pv(tmem + kTmemO0, tmem + kTmemS0, ring_addr(vit), j == 0);
-        if (!more) ptx::mma_commit(bar(kBarOFull + 0));
-        if (more) {
-          if (!(ok = ring_wait(kit))) break;
-          issue_s(tmem + kTmemS0, sQ, ring_addr(kit));
+        auto ring_wait = [&](int it) -> bool {
+          const bool r = wait_bounded(bar(kBarKvFull + it % kStages), (it / kStages) & 1, abort_flag,
+                                      p.timeout_ns, true);
+          ptx::tc_fence_after();
+          return r;
+        };
+        auto ring_addr = [&](int it) -> uint32_t { return sRing + (it % kStages) * kTileBytes; };
+        if (ok) ok = ring_wait(0);
+        if (ok) {
+          issue_s(tmem + kTmemS0, sQ, ring_addr(0));
           ptx::mma_commit(bar(kBarSFull + 0));
-        }
-        if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
-        ptx::tc_fence_after();
-        issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, ring_addr(vit), j == 0);
-        ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
-        if (!more) ptx::mma_commit(bar(kBarOFull + 1));
-        if (more) {
-          issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(kit));
+          issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(0));
           ptx::mma_commit(bar(kBarSFull + 1));
-          ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+          ptx::mma_commit(bar(kBarKvEmpty + 0));
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int vit = 2 * j + 1;
+          const int kit = 2 * j + 2;
+          const bool more = j + 1 < n_kv;
+          if (!(ok = ring_wait(vit))) break;
+          if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
+          ptx::tc_fence_after();
+          issue_pv(tmem + kTmemO0, tmem + kTmemS0, ring_addr(vit));
+          if (!more) ptx::mma_commit(bar(kBarOFull + 0));
+          if (more) {
+            if (!(ok = ring_wait(kit))) break;
+            issue_s(tmem + kTmemS0, sQ, ring_addr(kit));
+            ptx::mma_commit(bar(kBarSFull + 0));
+          }
+          if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
+          ptx::tc_fence_after();
+          issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, ring_addr(vit));
+          ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
+          if (!more) ptx::mma_commit(bar(kBarOFull + 1));
+          if (more) {
+            issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(kit));
+            ptx::mma_commit(bar(kBarSFull + 1));
+            ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+          }
+        }
+        if (!ok) {
+          // Abort: wait until every MMA issued so far has finished.
+          ptx::mma_commit(bar(kBarDrain));
+          wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
         }
       }
-      if (!ok) {
-        // Abort: wait until every MMA issued so far has finished.
-        ptx::mma_commit(bar(kBarDrain));
-        wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
-      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= kSoftmaxWarp0) {
+  } else {
+    ptx::setmaxnreg_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax + epilogue
     const int t = (warp - kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;                    // TMEM lane quarter of this warp
@@ -406,6 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float neg_inf = -__int_as_float(0x7F800000);
     float m_used = neg_inf;
     float l = 0.f;
+    float acc[kD];
+#pragma unroll
+    for (int i = 0; i < kD; ++i) acc[i] = 0.f;
     bool ok = true;
 
     for (int j = 0; j < n_kv; ++j) {
@@ -420,13 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_tile = ext * c;
       const bool need = m_tile > m_used + kTau;  // false for NaN
-      if (j > 0 && __any_sync(0xFFFFFFFFu, need)) {
-        // O holds every product up to key tile j-1 and nothing newer: the MMA
-        // that wrote S_j was issued after PV_{j-1}, and PV_j waits for P_j.
-        scale_o(tO, need ? ptx::ex2(m_used - m_tile) : 1.0f);
+      const float f = need ? ptx::ex2(m_used - m_tile) : 1.0f;  // 0 when m_used = -Inf
+      if (j > 0) {
+        // The TMEM accumulator holds exactly key tile j-1: the MMA that wrote S_j
+        // was issued after PV_{j-1}, and PV_j waits for P_j.
+        fold_tile(tO, acc, __any_sync(0xFFFFFFFFu, need), f);
       }
       if (need) {
-        l *= ptx::ex2(m_used - m_tile);
+        l *= f;
         m_used = m_tile;
       }
       const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
@@ -439,20 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
     if (ok) {
       ptx::tc_fence_after();
+      fold_tile(tO, acc, false, 1.0f);
       // Normalise, round, stage in the (now free) Q tile buffer with the TMA
       // 128-byte swizzle, and store this warp's 32 rows with two TMA boxes.
       const uint32_t stage_base = sQ + t * kTileBytes;
       const int mode = p.mode;
+      const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tO + 32 * ch, r);
-        ptx::tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float o0 = __fdiv_rn(__uint_as_float(r[2 * i]), l);
-          const float o1 = __fdiv_rn(__uint_as_float(r[2 * i + 1]), l);
+          const float o0 = acc[32 * ch + 2 * i] * inv_l;
+          const float o1 = acc[32 * ch + 2 * i + 1] * inv_l;
           w[i] = round_bf16_bits(o0, mode) | (round_bf16_bits(o1, mode) << 16);
         }
         const uint32_t half_base = stage_base + (ch >> 1) * kHalfBytes + row * 128;
