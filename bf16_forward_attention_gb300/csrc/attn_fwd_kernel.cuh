@@ -13,7 +13,7 @@
 //   warps 4-7   softmax + epilogue of query tile 0 (one TMEM lane = one row)
 //   warps 8-11  softmax + epilogue of query tile 1
 // The launch gives every thread 168 registers; the first warpgroup hands most of
-// its share to the two softmax warpgroups (56 + 2 * 224 = 3 * 168), which each
+// its share to the two softmax warpgroups (40 + 2 * 232 = 3 * 168), which each
 // keep a 128-float output row per thread.
 // Tensor memory (512 columns): O0 [0,128), O1 [128,256), S0/P0 [256,384),
 // S1/P1 [384,512). The MMA order per key tile j is
@@ -57,8 +57,8 @@ constexpr int kHalfBytes = kTileBytes / 2;  // 16 KiB: 128 rows x 64 columns (on
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kLaunchRegs = 168;     // per thread at launch: 65536 / 384, rounded to 8
-constexpr uint32_t kRegsLow = 56;    // producer / MMA warpgroup after the split
-constexpr uint32_t kRegsHigh = 224;  // each softmax warpgroup after the split
+constexpr uint32_t kRegsLow = 40;    // producer / MMA warpgroup after the split
+constexpr uint32_t kRegsHigh = 232;  // each softmax warpgroup after the split
 static_assert(kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (factor 256)
@@ -180,75 +180,130 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
   return u >> 16;
 }
 
-// Row extreme of one S tile: max if kPos (scale >= 0), else min (so that
-// scale * extreme is the max of the scaled logits). NaN-propagating. Columns
-// >= valid (key tail) are skipped when kMasked.
-template <bool kMasked, bool kPos>
-__device__ __forceinline__ float tile_extreme(uint32_t tS, int valid) {
-  const float init = kPos ? -__int_as_float(0x7F800000) : __int_as_float(0x7F800000);
-  float e[4] = {init, init, init, init};
-#pragma unroll 1
+// Pass A over one key tile. Folds the previous key tile's products (TMEM O)
+// into the register row when kFold, and returns the row max of S (NaN if any
+// element is NaN). Columns >= valid (the key tail) are skipped when kMasked.
+// Both 16-column loads of a chunk are issued before one wait.
+template <bool kMasked, bool kFold>
+__device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, float (&acc)[kD],
+                                              int valid) {
+  const float neg_inf = -__int_as_float(0x7F800000);
+  float e0 = neg_inf, e1 = neg_inf;
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t r[16], o[16];
+    ptx::tmem_ld16_nowait(tS + 16 * ch, r);
+    if (kFold) ptx::tmem_ld16_nowait(tO + 16 * ch, o);
+    ptx::tmem_wait_ld16(r);
+    if (kFold) ptx::reg_fence16(o);
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+      float s0 = __uint_as_float(r[i]), s1 = __uint_as_float(r[i + 1]);
+      float s2 = __uint_as_float(r[i + 2]), s3 = __uint_as_float(r[i + 3]);
+      if (kMasked) {
+        if (16 * ch + i >= valid) s0 = neg_inf;
+        if (16 * ch + i + 1 >= valid) s1 = neg_inf;
+        if (16 * ch + i + 2 >= valid) s2 = neg_inf;
+        if (16 * ch + i + 3 >= valid) s3 = neg_inf;
+      }
+      e0 = ptx::max3_nan(e0, s0, s1);
+      e1 = ptx::max3_nan(e1, s2, s3);
+    }
+    if (kFold) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[16 * ch + i] += __uint_as_float(o[i]);
+    }
+  }
+  return ptx::max_nan(e0, e1);
+}
+
+// Same for a negative scale, where the largest scaled logit comes from the
+// smallest S: returns the row min (NaN-propagating). Kept simple (rare case).
+template <bool kMasked>
+__device__ __forceinline__ float fold_and_min(uint32_t tS, uint32_t tO, float (&acc)[kD], int valid,
+                                              bool fold) {
+  const float pos_inf = __int_as_float(0x7F800000);
+  float e = pos_inf;
+#pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t r[32];
     ptx::tmem_ld32(tS + 32 * ch, r);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (kMasked && 32 * ch + i >= valid) continue;
-      const float s = __uint_as_float(r[i]);
-      e[i & 3] = kPos ? ptx::max_nan(e[i & 3], s) : ptx::min_nan(e[i & 3], s);
+      e = ptx::min_nan(e, __uint_as_float(r[i]));
+    }
+    if (fold) {
+      ptx::tmem_ld32(tO + 32 * ch, r);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[32 * ch + i] += __uint_as_float(r[i]);
     }
   }
-  if (kPos) return ptx::max_nan(ptx::max_nan(e[0], e[1]), ptx::max_nan(e[2], e[3]));
-  return ptx::min_nan(ptx::min_nan(e[0], e[1]), ptx::min_nan(e[2], e[3]));
+  return e;
 }
 
-// p = 2^(s*c - m_sub); writes P_hi / P_lo over the S columns (16-key chunks:
-// 8 columns of P_hi then 8 of P_lo); returns the sum of p.
+// p = 2^(s*c - m_sub) for one 16-key chunk; writes P_hi (8 columns) and P_lo
+// (8 columns) over the chunk's S columns; adds p into l.
+template <bool kMasked>
+__device__ __forceinline__ void exp_chunk(uint32_t tS, int u, const uint32_t (&r)[16], int valid,
+                                          float c, float m_sub, float (&l)[4]) {
+  const float neg_inf = -__int_as_float(0x7F800000);
+  uint32_t hi[8], lo[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float x0 = fmaf(__uint_as_float(r[2 * i]), c, -m_sub);
+    float x1 = fmaf(__uint_as_float(r[2 * i + 1]), c, -m_sub);
+    if (kMasked) {
+      if (16 * u + 2 * i >= valid) x0 = neg_inf;
+      if (16 * u + 2 * i + 1 >= valid) x1 = neg_inf;
+    }
+    const float p0 = ptx::ex2(x0);
+    const float p1 = ptx::ex2(x1);
+    l[(2 * i) & 3] += p0;
+    l[(2 * i + 1) & 3] += p1;
+    const uint32_t h = ptx::pack_bf16x2(p0, p1);
+    const float r0 = p0 - __uint_as_float(h << 16);
+    const float r1 = p1 - __uint_as_float(h & 0xFFFF0000u);
+    hi[i] = h;
+    lo[i] = ptx::pack_bf16x2(r0, r1);
+  }
+  ptx::tmem_st8(tS + 16 * u, hi);
+  ptx::tmem_st8(tS + 16 * u + 8, lo);
+}
+
+// Pass B over one key tile: exp, P split, row sum. The load of chunk u+1 is in
+// flight while chunk u is computed.
 template <bool kMasked>
 __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float m_sub) {
-  const float neg_inf = -__int_as_float(0x7F800000);
-  float l0 = 0.f, l1 = 0.f;
-#pragma unroll 1
-  for (int u = 0; u < 8; ++u) {
-    uint32_t r[16];
-    ptx::tmem_ld16(tS + 16 * u, r);
-    uint32_t hi[8], lo[8];
+  float l[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t ra[16], rb[16];
+  ptx::tmem_ld16_nowait(tS, ra);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float x0 = fmaf(__uint_as_float(r[2 * i]), c, -m_sub);
-      float x1 = fmaf(__uint_as_float(r[2 * i + 1]), c, -m_sub);
-      if (kMasked) {
-        if (16 * u + 2 * i >= valid) x0 = neg_inf;
-        if (16 * u + 2 * i + 1 >= valid) x1 = neg_inf;
-      }
-      const float p0 = ptx::ex2(x0);
-      const float p1 = ptx::ex2(x1);
-      l0 += p0;
-      l1 += p1;
-      const uint32_t h = ptx::pack_bf16x2(p0, p1);
-      const float r0 = p0 - __uint_as_float(h << 16);
-      const float r1 = p1 - __uint_as_float(h & 0xFFFF0000u);
-      hi[i] = h;
-      lo[i] = ptx::pack_bf16x2(r0, r1);
-    }
-    ptx::tmem_st8(tS + 16 * u, hi);
-    ptx::tmem_st8(tS + 16 * u + 8, lo);
+  for (int u = 0; u < 8; u += 2) {
+    ptx::tmem_wait_ld16(ra);
+    ptx::tmem_ld16_nowait(tS + 16 * (u + 1), rb);
+    exp_chunk<kMasked>(tS, u, ra, valid, c, m_sub, l);
+    ptx::tmem_wait_ld16(rb);
+    if (u + 2 < 8) ptx::tmem_ld16_nowait(tS + 16 * (u + 2), ra);
+    exp_chunk<kMasked>(tS, u + 1, rb, valid, c, m_sub, l);
   }
-  return l0 + l1;
+  return (l[0] + l[1]) + (l[2] + l[3]);
 }
 
-// acc += O (the finished key tile's products), then acc *= f when rescaling.
-__device__ __forceinline__ void fold_tile(uint32_t tO, float (&acc)[kD], bool rescale, float f) {
+// acc *= f (the rare lazy rescale).
+__device__ __forceinline__ void rescale_row(float (&acc)[kD], float f) {
+#pragma unroll
+  for (int i = 0; i < kD; ++i) acc[i] *= f;
+}
+
+// acc += O (the last key tile's products; epilogue).
+__device__ __forceinline__ void fold_last(uint32_t tO, float (&acc)[kD]) {
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t r[32];
     ptx::tmem_ld32(tO + 32 * ch, r);
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[32 * ch + i] += __uint_as_float(r[i]);
-  }
-  if (rescale) {
-#pragma unroll
-    for (int i = 0; i < kD; ++i) acc[i] *= f;
   }
 }
 
@@ -429,21 +484,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(bar(kBarSFull + t), j & 1, abort_flag, p.timeout_ns))) break;
       ptx::tc_fence_after();
       const bool last = (j == n_kv - 1) && (p.kv_tail < kBN);
+      // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
+      // holds exactly that tile: the MMA that wrote S_j was issued after
+      // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
       float ext;
-      if (last) {
-        ext = pos ? tile_extreme<true, true>(tS, p.kv_tail) : tile_extreme<true, false>(tS, p.kv_tail);
+      if (pos) {
+        if (j == 0) {
+          ext = last ? fold_and_max<true, false>(tS, tO, acc, p.kv_tail)
+                     : fold_and_max<false, false>(tS, tO, acc, kBN);
+        } else {
+          ext = last ? fold_and_max<true, true>(tS, tO, acc, p.kv_tail)
+                     : fold_and_max<false, true>(tS, tO, acc, kBN);
+        }
       } else {
-        ext = pos ? tile_extreme<false, true>(tS, kBN) : tile_extreme<false, false>(tS, kBN);
+        ext = last ? fold_and_min<true>(tS, tO, acc, p.kv_tail, j > 0)
+                   : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
       }
       const float m_tile = ext * c;
       const bool need = m_tile > m_used + kTau;  // false for NaN
-      const float f = need ? ptx::ex2(m_used - m_tile) : 1.0f;  // 0 when m_used = -Inf
-      if (j > 0) {
-        // The TMEM accumulator holds exactly key tile j-1: the MMA that wrote S_j
-        // was issued after PV_{j-1}, and PV_j waits for P_j.
-        fold_tile(tO, acc, __any_sync(0xFFFFFFFFu, need), f);
-      }
       if (need) {
+        const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+        if (j > 0) rescale_row(acc, f);
         l *= f;
         m_used = m_tile;
       }
@@ -457,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
     if (ok) {
       ptx::tc_fence_after();
-      fold_tile(tO, acc, false, 1.0f);
+      fold_last(tO, acc);
       // Normalise, round, stage in the (now free) Q tile buffer with the TMA
       // 128-byte swizzle, and store this warp's 32 rows with two TMA boxes.
       const uint32_t stage_base = sQ + t * kTileBytes;
