@@ -43,6 +43,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ptx.cuh"
 
 namespace attn {
@@ -100,11 +102,17 @@ struct Params {
 __device__ unsigned int g_attn_status;
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start,
-// leading and stride byte offsets in 16-byte units, version 1, layout 2).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+// leading and stride byte offsets in 16-byte units, version 1, layout 2). Every
+// operand here has a 1024-byte stride between 8-row groups, so the upper word is
+// one constant and only the lower word (start address, leading offset) varies.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16);
+}
+
+__device__ __forceinline__ uint64_t desc_of(uint32_t lo) {
+  return (static_cast<uint64_t>(kDescHi) << 32) | lo;
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
@@ -143,30 +151,43 @@ __device__ __forceinline__ void tma_coords(int layout, int s, int h, int& c1, in
   }
 }
 
+// Moving an operand's start address by b bytes adds b >> 4 to the descriptor's
+// lower word: the address field holds bits 4..17 and every shared address here
+// is below 256 KiB, so the add never carries out of the field.
+
 // S = Q K_j^T: 8 MMAs of K = 16 over head_dim; both operands K-major SW128.
-__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem) {
+// Step kk starts 32 bytes further into a 128-byte swizzle row; steps 4..7 use
+// the second 64-column half, 16 KiB further.
+template <int... kK>
+__device__ __forceinline__ void issue_s_seq(uint32_t tmem_d, uint32_t q_lo, uint32_t k_lo,
+                                            std::integer_sequence<int, kK...>) {
   constexpr uint32_t idesc = idesc_bf16(kBM, kBN, 0);
-#pragma unroll 1
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    ptx::mma_ss(tmem_d, desc_sw128(q_smem + off, 16, 1024), desc_sw128(k_smem + off, 16, 1024),
-                idesc, kk > 0 ? 1u : 0u);
-  }
+  (ptx::mma_ss_imm<((kK >> 2) << 10) + ((kK & 3) << 1), ((kK >> 2) << 10) + ((kK & 3) << 1)>(
+       tmem_d, q_lo, k_lo, kDescHi, idesc, kK > 0 ? 1u : 0u),
+   ...);
+}
+
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_lo, uint32_t k_lo) {
+  issue_s_seq(tmem_d, q_lo, k_lo, std::make_integer_sequence<int, 8>{});
 }
 
 // O_j = P_hi V_j + P_lo V_j into a fresh accumulator. P is in TMEM (A operand):
 // the 16 columns of key chunk u (keys 16u..16u+15) hold P_hi in their first 8
 // and P_lo in their last 8 columns, two bf16 per column. V_j (keys x head_dim,
 // head_dim contiguous) is the B operand in MN-major SW128: 8-key groups 1024 B
-// apart, the two 64-column halves 16 KiB apart.
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem) {
+// apart, the two 64-column halves 16 KiB apart (the leading offset); 16 keys
+// are 2048 bytes.
+template <int... kK>
+__device__ __forceinline__ void issue_pv_seq(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
+                                             std::integer_sequence<int, kK...>) {
   constexpr uint32_t idesc = idesc_bf16(kBM, kD, 1);
-#pragma unroll 1
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t bd = desc_sw128(v_smem + 2048 * kk, kHalfBytes, 1024);
-    ptx::mma_ts(tmem_o, tmem_p + 16 * kk, bd, idesc, kk == 0 ? 0u : 1u);
-    ptx::mma_ts(tmem_o, tmem_p + 16 * kk + 8, bd, idesc, 1u);
-  }
+  ((ptx::mma_ts_imm<16 * kK, (kK << 7)>(tmem_o, tmem_p, v_lo, kDescHi, idesc, kK == 0 ? 0u : 1u),
+    ptx::mma_ts_imm<16 * kK + 8, (kK << 7)>(tmem_o, tmem_p, v_lo, kDescHi, idesc, 1u)),
+   ...);
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo) {
+  issue_pv_seq(tmem_o, tmem_p, v_lo, std::make_integer_sequence<int, 8>{});
 }
 
 __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
@@ -419,12 +440,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           return r;
         };
-        auto ring_addr = [&](int it) -> uint32_t { return sRing + (it % kStages) * kTileBytes; };
+        // Ring stage descriptors: K tiles are K-major B operands, V tiles MN-major.
+        auto k_desc = [&](int it) -> uint32_t {
+          return desc_lo(sRing + (it % kStages) * kTileBytes, 16);
+        };
+        auto v_desc = [&](int it) -> uint32_t {
+          return desc_lo(sRing + (it % kStages) * kTileBytes, kHalfBytes);
+        };
+        const uint32_t q0_desc = desc_lo(sQ, 16);
+        const uint32_t q1_desc = desc_lo(sQ + kTileBytes, 16);
         if (ok) ok = ring_wait(0);
         if (ok) {
-          issue_s(tmem + kTmemS0, sQ, ring_addr(0));
+          issue_s(tmem + kTmemS0, q0_desc, k_desc(0));
           ptx::mma_commit(bar(kBarSFull + 0));
-          issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(0));
+          issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(0));
           ptx::mma_commit(bar(kBarSFull + 1));
           ptx::mma_commit(bar(kBarKvEmpty + 0));
         }
@@ -435,20 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = ring_wait(vit))) break;
           if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
           ptx::tc_fence_after();
-          issue_pv(tmem + kTmemO0, tmem + kTmemS0, ring_addr(vit));
+          issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit));
           if (!more) ptx::mma_commit(bar(kBarOFull + 0));
           if (more) {
             if (!(ok = ring_wait(kit))) break;
-            issue_s(tmem + kTmemS0, sQ, ring_addr(kit));
+            issue_s(tmem + kTmemS0, q0_desc, k_desc(kit));
             ptx::mma_commit(bar(kBarSFull + 0));
           }
           if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
           ptx::tc_fence_after();
-          issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, ring_addr(vit));
+          issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit));
           ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
           if (!more) ptx::mma_commit(bar(kBarOFull + 1));
           if (more) {
-            issue_s(tmem + kTmemS0 + 128, sQ + kTileBytes, ring_addr(kit));
+            issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(kit));
             ptx::mma_commit(bar(kBarSFull + 1));
             ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
           }

@@ -139,6 +139,36 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Same two MMAs with the descriptors built inside the asm statement from a
+// 32-bit lower word plus an immediate offset (16-byte units) and the shared upper
+// word, so that between MMAs no 64-bit descriptor occupies registers and each
+// MMA costs the issuing thread only a few instructions.
+template <uint32_t kAOff, uint32_t kBOff>
+__device__ __forceinline__ void mma_ss_imm(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t.reg .pred p;\n\t"
+      "add.u32 al, %1, %6;\n\tadd.u32 bl, %2, %7;\n\t"
+      "mov.b64 ad, {al, %3};\n\tmov.b64 bd, {bl, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "n"(kAOff), "n"(kBOff)
+      : "memory");
+}
+
+template <uint32_t kAColOff, uint32_t kBOff>
+__device__ __forceinline__ void mma_ts_imm(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .b32 at, bl;\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
+      "add.u32 at, %1, %6;\n\tadd.u32 bl, %2, %7;\n\t"
+      "mov.b64 bd, {bl, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "n"(kAColOff), "n"(kBOff)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -276,6 +306,36 @@ __device__ __forceinline__ float min_nan(float a, float b) {
   float y;
   asm("min.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
   return y;
+}
+
+// Packed pairs of fp32 (one 64-bit register pair; `lo` is the first element).
+// The f32x2 instructions round each lane to nearest like their scalar forms.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in bits 0..15.
