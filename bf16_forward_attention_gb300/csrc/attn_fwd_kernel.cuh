@@ -201,13 +201,16 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
   return u >> 16;
 }
 
+// The running output row of a softmax thread: 128 fp32 as 64 packed pairs
+// (column 2i in the low half of pair i), updated with packed f32x2 arithmetic.
+using Row = uint64_t[kD / 2];
+
 // Pass A over one key tile. Folds the previous key tile's products (TMEM O)
 // into the register row when kFold, and returns the row max of S (NaN if any
 // element is NaN). Columns >= valid (the key tail) are skipped when kMasked.
 // Both 16-column loads of a chunk are issued before one wait.
 template <bool kMasked, bool kFold>
-__device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, float (&acc)[kD],
-                                              int valid) {
+__device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, Row& acc, int valid) {
   const float neg_inf = -__int_as_float(0x7F800000);
   float e0 = neg_inf, e1 = neg_inf;
 #pragma unroll
@@ -232,7 +235,9 @@ __device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, float (&
     }
     if (kFold) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[16 * ch + i] += __uint_as_float(o[i]);
+      for (int i = 0; i < 8; ++i)
+        acc[8 * ch + i] = ptx::f2_add(
+            acc[8 * ch + i], ptx::f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])));
     }
   }
   return ptx::max_nan(e0, e1);
@@ -241,7 +246,7 @@ __device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, float (&
 // Same for a negative scale, where the largest scaled logit comes from the
 // smallest S: returns the row min (NaN-propagating). Kept simple (rare case).
 template <bool kMasked>
-__device__ __forceinline__ float fold_and_min(uint32_t tS, uint32_t tO, float (&acc)[kD], int valid,
+__device__ __forceinline__ float fold_and_min(uint32_t tS, uint32_t tO, Row& acc, int valid,
                                               bool fold) {
   const float pos_inf = __int_as_float(0x7F800000);
   float e = pos_inf;
@@ -257,34 +262,42 @@ __device__ __forceinline__ float fold_and_min(uint32_t tS, uint32_t tO, float (&
     if (fold) {
       ptx::tmem_ld32(tO + 32 * ch, r);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[32 * ch + i] += __uint_as_float(r[i]);
+      for (int i = 0; i < 16; ++i)
+        acc[16 * ch + i] = ptx::f2_add(
+            acc[16 * ch + i], ptx::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])));
     }
   }
   return e;
 }
 
 // p = 2^(s*c - m_sub) for one 16-key chunk; writes P_hi (8 columns) and P_lo
-// (8 columns) over the chunk's S columns; adds p into l.
+// (8 columns) over the chunk's S columns; adds p into the pair sums l. Pairs of
+// columns go through packed f32x2 instructions.
 template <bool kMasked>
 __device__ __forceinline__ void exp_chunk(uint32_t tS, int u, const uint32_t (&r)[16], int valid,
-                                          float c, float m_sub, float (&l)[4]) {
+                                          uint64_t c2, uint64_t neg_m2, uint64_t (&l)[2]) {
   const float neg_inf = -__int_as_float(0x7F800000);
   uint32_t hi[8], lo[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float x0 = fmaf(__uint_as_float(r[2 * i]), c, -m_sub);
-    float x1 = fmaf(__uint_as_float(r[2 * i + 1]), c, -m_sub);
+    const uint64_t x = ptx::f2_fma(
+        ptx::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, neg_m2);
+    float x0, x1;
+    ptx::f2_unpack(x, x0, x1);
     if (kMasked) {
       if (16 * u + 2 * i >= valid) x0 = neg_inf;
       if (16 * u + 2 * i + 1 >= valid) x1 = neg_inf;
     }
     const float p0 = ptx::ex2(x0);
     const float p1 = ptx::ex2(x1);
-    l[(2 * i) & 3] += p0;
-    l[(2 * i + 1) & 3] += p1;
+    const uint64_t p2 = ptx::f2_pack(p0, p1);
+    l[i & 1] = ptx::f2_add(l[i & 1], p2);
     const uint32_t h = ptx::pack_bf16x2(p0, p1);
-    const float r0 = p0 - __uint_as_float(h << 16);
-    const float r1 = p1 - __uint_as_float(h & 0xFFFF0000u);
+    // p - bf16(p) is exact in fp32; one packed subtraction per pair.
+    const uint64_t res =
+        ptx::f2_sub(p2, ptx::f2_pack(__uint_as_float(h << 16), __uint_as_float(h & 0xFFFF0000u)));
+    float r0, r1;
+    ptx::f2_unpack(res, r0, r1);
     hi[i] = h;
     lo[i] = ptx::pack_bf16x2(r0, r1);
   }
@@ -296,35 +309,43 @@ __device__ __forceinline__ void exp_chunk(uint32_t tS, int u, const uint32_t (&r
 // flight while chunk u is computed.
 template <bool kMasked>
 __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float m_sub) {
-  float l[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint64_t c2 = ptx::f2_pack(c, c);
+  const uint64_t neg_m2 = ptx::f2_pack(-m_sub, -m_sub);
+  uint64_t l[2] = {0, 0};
   uint32_t ra[16], rb[16];
   ptx::tmem_ld16_nowait(tS, ra);
 #pragma unroll
   for (int u = 0; u < 8; u += 2) {
     ptx::tmem_wait_ld16(ra);
     ptx::tmem_ld16_nowait(tS + 16 * (u + 1), rb);
-    exp_chunk<kMasked>(tS, u, ra, valid, c, m_sub, l);
+    exp_chunk<kMasked>(tS, u, ra, valid, c2, neg_m2, l);
     ptx::tmem_wait_ld16(rb);
     if (u + 2 < 8) ptx::tmem_ld16_nowait(tS + 16 * (u + 2), ra);
-    exp_chunk<kMasked>(tS, u + 1, rb, valid, c, m_sub, l);
+    exp_chunk<kMasked>(tS, u + 1, rb, valid, c2, neg_m2, l);
   }
-  return (l[0] + l[1]) + (l[2] + l[3]);
+  float a0, a1, b0, b1;
+  ptx::f2_unpack(l[0], a0, a1);
+  ptx::f2_unpack(l[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
 }
 
 // acc *= f (the rare lazy rescale).
-__device__ __forceinline__ void rescale_row(float (&acc)[kD], float f) {
+__device__ __forceinline__ void rescale_row(Row& acc, float f) {
+  const uint64_t f2 = ptx::f2_pack(f, f);
 #pragma unroll
-  for (int i = 0; i < kD; ++i) acc[i] *= f;
+  for (int i = 0; i < kD / 2; ++i) acc[i] = ptx::f2_mul(acc[i], f2);
 }
 
 // acc += O (the last key tile's products; epilogue).
-__device__ __forceinline__ void fold_last(uint32_t tO, float (&acc)[kD]) {
+__device__ __forceinline__ void fold_last(uint32_t tO, Row& acc) {
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t r[32];
     ptx::tmem_ld32(tO + 32 * ch, r);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[32 * ch + i] += __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i)
+      acc[16 * ch + i] = ptx::f2_add(
+          acc[16 * ch + i], ptx::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])));
   }
 }
 
@@ -504,9 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float neg_inf = -__int_as_float(0x7F800000);
     float m_used = neg_inf;
     float l = 0.f;
-    float acc[kD];
+    Row acc;
 #pragma unroll
-    for (int i = 0; i < kD; ++i) acc[i] = 0.f;
+    for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
     bool ok = true;
 
     for (int j = 0; j < n_kv; ++j) {
@@ -553,13 +574,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t stage_base = sQ + t * kTileBytes;
       const int mode = p.mode;
       const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
+      const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float o0 = acc[32 * ch + 2 * i] * inv_l;
-          const float o1 = acc[32 * ch + 2 * i + 1] * inv_l;
+          float o0, o1;
+          ptx::f2_unpack(ptx::f2_mul(acc[16 * ch + i], inv2), o0, o1);
           w[i] = round_bf16_bits(o0, mode) | (round_bf16_bits(o1, mode) << 16);
         }
         const uint32_t half_base = stage_base + (ch >> 1) * kHalfBytes + row * 128;
