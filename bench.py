@@ -51,6 +51,24 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("bf16_forward_attention_gb300/csrc/attn_fwd_kernel.cuh",
+                  "bf16_forward_attention_gb300/csrc/ptx.cuh",
+                  "bf16_forward_attention_gb300/csrc/attn_fwd.cu")
+
+
+def _recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu record, if it was taken on
+    exactly the current kernel sources (else None: the counters are stale)."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["attn_fwd_kernel"][workload]
+        h = hashlib.sha256(b"".join(open(os.path.join(ROOT, p), "rb").read()
+                                    for p in KERNEL_SOURCES)).hexdigest()[:16]
+    except (OSError, KeyError, ValueError):
+        return None
+    return float(rec["dram_bytes_per_launch"]) if rec.get("sources_sha256_16") == h else None
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -300,7 +318,8 @@ def run_ours(args, w):
                       "p5": launch_ms[int(0.05 * (len(launch_ms) - 1))],
                       "p95": launch_ms[int(0.95 * (len(launch_ms) - 1))], "n": len(launch_ms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": args.traffic,
+                     "frac": achieved / peak,
+                     "traffic": args.traffic if args.traffic is not None else _recorded_traffic(w.name),
                      "peak_kind": f"{'sustained' if sustained else 'burst'} dense bf16 ({peak_src})",
                      "kernel": "attn_fwd_kernel",
                      "note": "achieved counts 4*B*H*Sq*Sk*d per launch; the kernel also runs the "
