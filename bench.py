@@ -76,6 +76,14 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist, device=None) -> float:
+    """Max of a per-rank float over the process group (the job is as slow as its
+    slowest rank). Works with NCCL (device tensor) and gloo (CPU tensor)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons every 200 ms."""
 
@@ -255,9 +263,7 @@ def run_ours(args, w):
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
     if dist:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     launch_ms = sorted(a.elapsed_time(b) for a, b in ev)
     clocks = sampler.stop() if rank == 0 else None
     if attn.attn_fwd_last_error() != attn.ATTN_OK:
