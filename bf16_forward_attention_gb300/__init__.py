@@ -59,6 +59,8 @@ def load_library() -> ctypes.CDLL:
     lib.attn_fwd_last_error.restype = ctypes.c_int
     lib.attn_fwd_version.argtypes = []
     lib.attn_fwd_version.restype = ctypes.c_int
+    lib.attn_fwd_timeout_selftest.argtypes = lib.attn_fwd.argtypes + [ctypes.c_uint64]
+    lib.attn_fwd_timeout_selftest.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -72,6 +74,16 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, 
     """Direct call of the C entry point ``attn_fwd``; returns its status code."""
     return load_library().attn_fwd(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq, Sk, d,
                                    ctypes.c_float(scale), rounding_mode, stream)
+
+
+def attn_fwd_timeout_selftest_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int,
+                                  B: int, H: int, Sq: int, Sk: int, d: int, scale: float,
+                                  rounding_mode: int, stream: int, timeout_ns: int) -> int:
+    """Direct call of ``attn_fwd_timeout_selftest`` (a launch whose device-side
+    wait must time out; see include/attn_fwd.h)."""
+    return load_library().attn_fwd_timeout_selftest(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq,
+                                                    Sk, d, ctypes.c_float(scale), rounding_mode,
+                                                    stream, timeout_ns)
 
 
 def attn_fwd_last_error() -> int:
@@ -128,5 +140,5 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
     return out
 
 
-__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "status_str", "load_library",
+__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

@@ -130,9 +130,13 @@ const char* attn_status_str(int status) {
 
 int attn_fwd_version(void) { return kVersion; }
 
-int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
-             int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
-             void* stream) {
+}  // extern "C"
+
+namespace {
+
+int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
+                  int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
+                  void* stream, unsigned long long timeout_ns, int withhold_s0) {
   // ---- host-side validation (nothing is launched on failure)
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
@@ -180,13 +184,33 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
   p.layout = layout;
   p.mode = rounding_mode;
   p.c = scale * 1.4426950408889634f;
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = timeout_ns;
+  p.withhold_s0 = withhold_s0;
 
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs);
   attn::attn_fwd_kernel<<<grid, attn::kThreads, attn::kSmemBytes,
                           static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
+             int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
+             void* stream) {
+  return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
+                       kTimeoutNs, 0);
+}
+
+int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void* out, int layout,
+                              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                              int rounding_mode, void* stream, uint64_t timeout_ns) {
+  if (timeout_ns == 0 || timeout_ns > kTimeoutNs) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
+                       timeout_ns, 1);
 }
 
 int attn_fwd_last_error(void) {

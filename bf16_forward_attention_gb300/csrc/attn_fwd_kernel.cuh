@@ -96,6 +96,7 @@ struct Params {
   int mode;      // 0 = RTNE, 1 = RTNA, 2 = RTZ
   float c;       // scale * log2(e)
   unsigned long long timeout_ns;
+  int withhold_s0;  // self-test of the timeout path: never signal query tile 0's first S
 };
 
 // Bit 0: some wait timed out.
@@ -416,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ producer
       if (lane == 0) {
         int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
-        bool ok = true;
         int c1, c2;
         ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
         for (int t = 0; t < kQTiles; ++t) {
@@ -428,10 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < 2 * n_kv; ++it) {
           const int stage = it % kStages;
           const uint32_t parity = ((it / kStages) & 1) ^ 1;
-          if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) {
-            ok = false;
-            break;
-          }
+          if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
           const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
           tma_coords(p.layout, (it >> 1) * kBN, head, c1, c2);
           ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
@@ -440,13 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              64 * hf, c1, c2, batch);
           ++issued;
         }
-        if (!ok) {
-          // Abort: let every copy this thread started land before the CTA exits.
-          wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
-          for (int s = 0; s < kStages && s < issued; ++s) {
-            const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
-            wait_bounded(bar(kBarKvFull + s), (fills - 1) & 1, abort_flag, p.timeout_ns, false);
-          }
+        // Let every copy this thread started land before the CTA can exit. On
+        // the normal path these phases have long completed; after an abort the
+        // consumer may never have waited for them.
+        wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
+        for (int s = 0; s < kStages && s < issued; ++s) {
+          const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
+          wait_bounded(bar(kBarKvFull + s), (fills - 1) & 1, abort_flag, p.timeout_ns, false);
         }
       }
       __syncwarp();
@@ -473,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = ring_wait(0);
         if (ok) {
           issue_s(tmem + kTmemS0, q0_desc, k_desc(0));
-          ptx::mma_commit(bar(kBarSFull + 0));
+          if (!p.withhold_s0) ptx::mma_commit(bar(kBarSFull + 0));
           issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(0));
           ptx::mma_commit(bar(kBarSFull + 1));
           ptx::mma_commit(bar(kBarKvEmpty + 0));
@@ -503,11 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
           }
         }
-        if (!ok) {
-          // Abort: wait until every MMA issued so far has finished.
-          ptx::mma_commit(bar(kBarDrain));
-          wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
-        }
+        // Wait until every MMA issued so far has finished (immediate on the normal
+        // path, where the softmax warps have already waited for the last ones).
+        ptx::mma_commit(bar(kBarDrain));
+        wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
       }
       __syncwarp();
     }

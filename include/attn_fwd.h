@@ -91,6 +91,22 @@ const char* attn_status_str(int status);
  */
 int attn_fwd_last_error(void);
 
+/*
+ * attn_fwd_timeout_selftest - exercises the failure path on a real GPU.
+ *
+ * Same arguments, checks and launch as attn_fwd, plus a wait limit in
+ * nanoseconds (1 .. 2e9), but the kernel withholds one of its own internal
+ * signals (the tensor-core warp never announces query tile 0's first S tile),
+ * so a device-side wait must run out. Every role of the kernel then stops,
+ * waits for the copies and matrix products it started, frees its tensor memory
+ * and returns; no output is written (`out` keeps its old contents) and after the
+ * stream is synchronized attn_fwd_last_error() reports ATTN_ERR_TIMEOUT. The
+ * CUDA context stays usable. Returns ATTN_OK if the launch went out.
+ */
+int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void* out, int layout,
+                              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                              int rounding_mode, void* stream, uint64_t timeout_ns);
+
 /* Library version, as MAJOR*10000 + MINOR*100 + PATCH. */
 int attn_fwd_version(void);
 

@@ -81,6 +81,14 @@ def test_host_validation(lib, kw, status):
     assert _call(**kw) == status
 
 
+def test_timeout_selftest_validation(lib):
+    args = (A, 2 * A, 3 * A, 4 * A, 0, 1, 2, 256, 256, 128, 0.088, 0)
+    assert attn.attn_fwd_timeout_selftest_raw(*args, 0, 0) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_timeout_selftest_raw(*args, 0, 3_000_000_000) == attn.ATTN_ERR_INVALID_ARG
+    bad = (0,) + args[1:]
+    assert attn.attn_fwd_timeout_selftest_raw(*bad, 0, 10_000_000) == attn.ATTN_ERR_INVALID_ARG
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
 def test_valid_call_without_gpu_reports_no_device(lib):
     assert _call() == attn.ATTN_ERR_NO_DEVICE

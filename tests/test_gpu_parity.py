@@ -7,6 +7,8 @@ the benchmark and are compared on sampled rows (the first and last rows of tiles
 plus random rows), with the NaN/Inf pattern of the stress case checked over the
 whole tensor against its closed form.
 """
+import json
+
 import numpy as np
 import pytest
 import torch
@@ -188,6 +190,7 @@ def test_full_size_sampled(name):
         ob = to_bhsd(bits_of(out), w.layout)
         got = np.concatenate([ob[b, h, rows] for b, h, rows in plan])
         stats = compare(got, exact, mode)
+        print(f"\nPARITY {name} {mode}: " + json.dumps(stats))
         assert_parity(stats, 8e-3 if w.qk_std == 1.0 else None)
         if w.specials:
             mask = _closed_form_nonfinite_rows(w, q)
