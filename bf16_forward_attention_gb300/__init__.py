@@ -61,6 +61,15 @@ def load_library() -> ctypes.CDLL:
     lib.attn_fwd_version.restype = ctypes.c_int
     lib.attn_fwd_timeout_selftest.argtypes = lib.attn_fwd.argtypes + [ctypes.c_uint64]
     lib.attn_fwd_timeout_selftest.restype = ctypes.c_int
+    lib.attn_fwd_splitkv.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64, i64, i64,
+                                                             ctypes.c_float, ctypes.c_int,
+                                                             ctypes.c_int, ctypes.c_void_p, i64,
+                                                             ctypes.c_void_p]
+    lib.attn_fwd_splitkv.restype = ctypes.c_int
+    lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int]
+    lib.attn_fwd_splitkv_workspace_bytes.restype = i64
+    lib.attn_fwd_splitkv_num_splits.argtypes = [i64, i64, i64, i64]
+    lib.attn_fwd_splitkv_num_splits.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -84,6 +93,71 @@ def attn_fwd_timeout_selftest_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: i
     return load_library().attn_fwd_timeout_selftest(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq,
                                                     Sk, d, ctypes.c_float(scale), rounding_mode,
                                                     stream, timeout_ns)
+
+
+def attn_fwd_splitkv_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, B: int,
+                         H: int, Sq: int, Sk: int, d: int, scale: float, rounding_mode: int,
+                         num_splits: int, workspace_ptr: int, workspace_bytes: int,
+                         stream: int) -> int:
+    """Direct call of the C entry point ``attn_fwd_splitkv``; returns its status."""
+    return load_library().attn_fwd_splitkv(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq, Sk, d,
+                                           ctypes.c_float(scale), rounding_mode, num_splits,
+                                           workspace_ptr, workspace_bytes, stream)
+
+
+def splitkv_workspace_bytes(B: int, H: int, Sq: int, Sk: int, num_splits: int, d: int = 128) -> int:
+    n = load_library().attn_fwd_splitkv_workspace_bytes(B, H, Sq, Sk, d, num_splits)
+    if n < 0:
+        raise AttnError(int(n), status_str(int(n)))
+    return int(n)
+
+
+def splitkv_num_splits(B: int, H: int, Sq: int, Sk: int) -> int:
+    n = load_library().attn_fwd_splitkv_num_splits(B, H, Sq, Sk)
+    if n < 0:
+        raise AttnError(int(n), status_str(int(n)))
+    return int(n)
+
+
+def attn_fwd_splitkv(q, k, v, *, num_splits: int | None = None, layout: str = "bhsd",
+                     scale: float | None = None, rounding: str = "rtne", out=None,
+                     workspace=None):
+    """attn_fwd with the key range split over several CTAs (see include/attn_fwd.h).
+
+    ``workspace``: a CUDA tensor of at least ``splitkv_workspace_bytes(...)`` bytes;
+    allocated here if not given (the C entry point itself never allocates).
+    """
+    import torch
+
+    if layout not in LAYOUTS or rounding not in ROUNDINGS:
+        raise ValueError("unknown layout or rounding mode")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, H, Sq, D = _dims(q, layout)
+    Bk, Hk, Sk, Dk = _dims(k, layout)
+    if (Bk, Hk, Dk) != (B, H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch")
+    if num_splits is None:
+        num_splits = splitkv_num_splits(B, H, Sq, Sk)
+    need = splitkv_workspace_bytes(B, H, Sq, Sk, num_splits, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  LAYOUTS[layout], B, H, Sq, Sk, D, float(scale),
+                                  ROUNDINGS[rounding], num_splits, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, status_str(st))
+    return out
 
 
 def attn_fwd_last_error() -> int:
@@ -140,5 +214,7 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
     return out
 
 
-__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw", "status_str", "load_library",
+__all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw",
+           "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
+           "splitkv_num_splits", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

@@ -15,6 +15,7 @@
 
 #include "attn_fwd.h"
 #include "attn_fwd_kernel.cuh"
+#include "splitkv_combine.cuh"
 
 namespace {
 
@@ -55,7 +56,9 @@ int device_ready(int dev) {
     g_dev_state[dev] = ATTN_ERR_ARCH;
     return ATTN_ERR_ARCH;
   }
-  if (cudaFuncSetAttribute(attn::attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attn::attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           attn::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(attn::attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            attn::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
@@ -64,14 +67,17 @@ int device_ready(int dev) {
   // (setmaxnreg); the split only adds up if each thread starts with exactly
   // kLaunchRegs. A build with another count would make setmaxnreg.inc wait
   // forever, so it is refused here.
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, attn::attn_fwd_kernel) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_LAUNCH;
-  }
-  if (fa.numRegs != attn::kLaunchRegs) {
-    g_dev_state[dev] = ATTN_ERR_LAUNCH;
-    return ATTN_ERR_LAUNCH;
+  for (int i = 0; i < 2; ++i) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, i ? attn::attn_fwd_kernel<true> : attn::attn_fwd_kernel<false>) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
+    if (fa.numRegs != attn::kLaunchRegs) {
+      g_dev_state[dev] = ATTN_ERR_LAUNCH;
+      return ATTN_ERR_LAUNCH;
+    }
   }
   g_dev_state[dev] = 1;
   return ATTN_OK;
@@ -108,6 +114,15 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+int64_t kv_tiles_of(int64_t Sk) { return (Sk + attn::kBN - 1) / attn::kBN; }
+int64_t qpairs_of(int64_t Sq) { return (Sq + 2 * attn::kBM - 1) / (2 * attn::kBM); }
+
+// Split workspace: unnormalised rows (128 fp32) then (reference max, row sum).
+int64_t splitkv_bytes(int64_t B, int64_t H, int64_t Sq, int64_t n_splits) {
+  const int64_t rows = n_splits * B * H * qpairs_of(Sq) * 2 * attn::kBM;
+  return rows * (attn::kD + 2) * 4;
+}
+
 }  // namespace
 
 extern "C" {
@@ -136,7 +151,8 @@ namespace {
 
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
                   int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
-                  void* stream, unsigned long long timeout_ns, int withhold_s0) {
+                  void* stream, unsigned long long timeout_ns, int withhold_s0, int n_splits,
+                  void* workspace, int64_t workspace_bytes) {
   // ---- host-side validation (nothing is launched on failure)
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
@@ -150,8 +166,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   const int64_t kStrideLim = int64_t(1) << 40;
   if (H > kStrideLim / 256 / Sq || H > kStrideLim / 256 / Sk) return ATTN_ERR_TOO_LARGE;
   if (B > (int64_t(1) << 62) / 256 / H / (Sq > Sk ? Sq : Sk)) return ATTN_ERR_TOO_LARGE;
-  const int64_t n_qpairs = (Sq + 2 * attn::kBM - 1) / (2 * attn::kBM);
-  if (B * H > kLim31 / n_qpairs) return ATTN_ERR_TOO_LARGE;
+  const int64_t n_qpairs = qpairs_of(Sq);
+  if (n_splits < 1 || n_splits > kv_tiles_of(Sk)) return ATTN_ERR_INVALID_ARG;
+  if (B * H > kLim31 / n_qpairs / n_splits) return ATTN_ERR_TOO_LARGE;
   const uintptr_t ormask = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                            reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
   if (ormask & 15u) return ATTN_ERR_MISALIGNED;
@@ -159,6 +176,14 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   if (overlaps(out, bytes_q, q, bytes_q) || overlaps(out, bytes_q, k, bytes_kv) ||
       overlaps(out, bytes_q, v, bytes_kv))
     return ATTN_ERR_ALIASING;
+  if (n_splits > 1) {
+    const int64_t need = splitkv_bytes(B, H, Sq, n_splits);
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return ATTN_ERR_MISALIGNED;
+    if (overlaps(workspace, need, q, bytes_q) || overlaps(workspace, need, k, bytes_kv) ||
+        overlaps(workspace, need, v, bytes_kv) || overlaps(workspace, need, out, bytes_q))
+      return ATTN_ERR_ALIASING;
+  }
 
   // ---- device
   int dev = -1;
@@ -179,17 +204,40 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.Sk = static_cast<int>(Sk);
   p.H = static_cast<int>(H);
   p.n_qpairs = static_cast<int>(n_qpairs);
-  p.n_kv = static_cast<int>((Sk + attn::kBN - 1) / attn::kBN);
-  p.kv_tail = static_cast<int>(Sk - int64_t(p.n_kv - 1) * attn::kBN);
+  p.kv_tiles = static_cast<int>(kv_tiles_of(Sk));
+  p.kv_tail = static_cast<int>(Sk - int64_t(p.kv_tiles - 1) * attn::kBN);
+  p.n_splits = n_splits;
+  p.BH = static_cast<int>(B * H);
+  p.sq_pad = static_cast<int>(n_qpairs * 2 * attn::kBM);
+  p.part_o = static_cast<float*>(workspace);
+  p.part_rl = n_splits > 1 ? p.part_o + static_cast<size_t>(n_splits) * B * H * p.sq_pad * attn::kD
+                           : nullptr;
   p.layout = layout;
   p.mode = rounding_mode;
   p.c = scale * 1.4426950408889634f;
   p.timeout_ns = timeout_ns;
   p.withhold_s0 = withhold_s0;
 
-  const unsigned grid = static_cast<unsigned>(B * H * n_qpairs);
-  attn::attn_fwd_kernel<<<grid, attn::kThreads, attn::kSmemBytes,
-                          static_cast<cudaStream_t>(stream)>>>(tq, tk, tv, to, p);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
+  if (n_splits == 1) {
+    attn::attn_fwd_kernel<false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+  } else {
+    attn::attn_fwd_kernel<true><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+    attn::CombineParams cp;
+    cp.part_o = p.part_o;
+    cp.part_rl = p.part_rl;
+    cp.out = static_cast<uint16_t*>(out);
+    cp.n_splits = n_splits;
+    cp.BH = p.BH;
+    cp.H = p.H;
+    cp.Sq = p.Sq;
+    cp.sq_pad = p.sq_pad;
+    cp.layout = layout;
+    cp.mode = rounding_mode;
+    attn::attn_splitkv_combine<<<dim3(static_cast<unsigned>(Sq), static_cast<unsigned>(B * H)),
+                                 attn::kD, 0, cs>>>(cp);
+  }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }
@@ -202,7 +250,44 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
              int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
              void* stream) {
   return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
-                       kTimeoutNs, 0);
+                       kTimeoutNs, 0, 1, nullptr, 0);
+}
+
+int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                                         int num_splits) {
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (num_splits > kv_tiles_of(Sk)) return ATTN_ERR_INVALID_ARG;
+  if (B > (int64_t(1) << 31) || H > (int64_t(1) << 31) || Sq > (int64_t(1) << 31))
+    return ATTN_ERR_TOO_LARGE;
+  if (num_splits == 1) return 0;
+  return splitkv_bytes(B, H, Sq, num_splits);
+}
+
+int attn_fwd_splitkv_num_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk) {
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  int sms = 152, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  else
+    cudaGetLastError();
+  const int64_t items = B * H * qpairs_of(Sq);
+  const int64_t tiles = kv_tiles_of(Sk);
+  if (items >= sms) return 1;
+  // Enough CTAs to fill the GPU once, keeping at least 4 key tiles per split.
+  int64_t s = (sms + items - 1) / items;
+  const int64_t max_s = tiles / 4 > 0 ? tiles / 4 : 1;
+  if (s > max_s) s = max_s;
+  if (s > 64) s = 64;
+  return static_cast<int>(s);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, int layout,
+                     int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                     int rounding_mode, int num_splits, void* workspace, int64_t workspace_bytes,
+                     void* stream) {
+  return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
+                       kTimeoutNs, 0, num_splits, workspace, workspace_bytes);
 }
 
 int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void* out, int layout,
@@ -210,7 +295,7 @@ int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void*
                               int rounding_mode, void* stream, uint64_t timeout_ns) {
   if (timeout_ns == 0 || timeout_ns > kTimeoutNs) return ATTN_ERR_INVALID_ARG;
   return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
-                       timeout_ns, 1);
+                       timeout_ns, 1, 1, nullptr, 0);
 }
 
 int attn_fwd_last_error(void) {

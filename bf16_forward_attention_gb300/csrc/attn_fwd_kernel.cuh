@@ -90,8 +90,13 @@ constexpr uint32_t kTmemO0 = 0, kTmemS0 = 256;
 struct Params {
   int Sq, Sk, H;
   int n_qpairs;  // ceil(Sq / 256)
-  int n_kv;      // ceil(Sk / 128)
+  int kv_tiles;  // ceil(Sk / 128)
   int kv_tail;   // valid keys in the last key tile, 1..128
+  int n_splits;  // key-range splits (1: whole range per CTA, bf16 output)
+  int BH;        // B * H
+  int sq_pad;    // n_qpairs * 256: row pitch of the split workspace
+  float* part_o;   // split workspace: [split][b*H + h][sq_pad][128] unnormalised O
+  float* part_rl;  // split workspace: [split][b*H + h][sq_pad][2] (reference max, row sum)
   int layout;    // 0 = BHSD, 1 = BSHD
   int mode;      // 0 = RTNE, 1 = RTNA, 2 = RTZ
   float c;       // scale * log2(e)
@@ -356,6 +361,35 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// The CTA's share of the work: (batch, head, query-tile pair, key split) and the
+// split's key tiles. Splits of one pair are adjacent in the grid, pairs of one
+// head are adjacent (so K/V of a head stay in L2). Recomputed by each role where
+// it is needed, rather than kept live across the softmax loop.
+struct Work {
+  int split, pair, bh, head, batch;
+  int tile0, n_kv;  // key tiles [tile0, tile0 + n_kv)
+  bool has_tail;    // this split holds the ragged last key tile
+};
+
+__device__ __forceinline__ Work work_of(const Params& p) {
+  Work w;
+  w.split = blockIdx.x % p.n_splits;
+  const int item = blockIdx.x / p.n_splits;
+  w.pair = item % p.n_qpairs;
+  w.bh = item / p.n_qpairs;
+  w.head = w.bh % p.H;
+  w.batch = w.bh / p.H;
+  const int base = p.kv_tiles / p.n_splits, rem = p.kv_tiles % p.n_splits;
+  w.tile0 = w.split * base + (w.split < rem ? w.split : rem);
+  w.n_kv = base + (w.split < rem ? 1 : 0);
+  w.has_tail = w.tile0 + w.n_kv == p.kv_tiles && p.kv_tail < kBN;
+  return w;
+}
+
+// kPartial: the CTA covers one split of the key range and writes its fp32 partial
+// result to the workspace (combined by attn_splitkv_combine); otherwise the CTA
+// covers all keys and stores bf16 output.
+template <bool kPartial>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -372,11 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x % p.n_qpairs;
-  const int bh = blockIdx.x / p.n_qpairs;
-  const int head = bh % p.H;
-  const int batch = bh / p.H;
-  const int n_kv = p.n_kv;
+
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(kBarQ), 1);
@@ -416,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
+        const Work wk = work_of(p);
+        const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
         int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
         int c1, c2;
         ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
@@ -430,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t parity = ((it / kStages) & 1) ^ 1;
           if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
           const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-          tma_coords(p.layout, (it >> 1) * kBN, head, c1, c2);
+          tma_coords(p.layout, (tile0 + (it >> 1)) * kBN, head, c1, c2);
           ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
             ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
@@ -450,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
+        const int n_kv = work_of(p).n_kv;
         bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
         ptx::tc_fence_after();
         auto ring_wait = [&](int it) -> bool {
@@ -525,11 +558,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
     bool ok = true;
+    const int n_kv = work_of(p).n_kv;  // key tiles of this CTA
 
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = warp_wait(bar(kBarSFull + t), j & 1, abort_flag, p.timeout_ns))) break;
       ptx::tc_fence_after();
-      const bool last = (j == n_kv - 1) && (p.kv_tail < kBN);
+      // The ragged key tile is the last tile of the last split. Written as tests
+      // of kernel parameters and the block index, which keeps the compiler's
+      // register allocation of this loop free of spills.
+      const bool last = (j == n_kv - 1) && (p.kv_tail < kBN) &&
+                        (!kPartial || static_cast<int>(blockIdx.x % p.n_splits) == p.n_splits - 1);
       // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
       // holds exactly that tile: the MMA that wrote S_j was issued after
       // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
@@ -562,7 +600,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
-    if (ok) {
+    const Work wk = work_of(p);
+    if (kPartial && ok) {
+      // Split epilogue: this row's unnormalised fp32 output, the running max it is
+      // relative to, and its row sum.
+      ptx::tc_fence_after();
+      fold_last(tO, acc);
+      const int q = (2 * wk.pair + t) * kBM + row;
+      if (q < p.Sq) {
+        const size_t r = (static_cast<size_t>(wk.split) * p.BH + wk.bh) * p.sq_pad + q;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + r * kD);
+#pragma unroll
+        for (int i = 0; i < kD / 4; ++i) {
+          float a0, a1, a2, a3;
+          ptx::f2_unpack(acc[2 * i], a0, a1);
+          ptx::f2_unpack(acc[2 * i + 1], a2, a3);
+          dst[i] = make_float4(a0, a1, a2, a3);
+        }
+        // The products are relative to m_used, or to 0 while it is -Inf (then no key
+        // had a finite logit and both sums are 0, or NaN).
+        reinterpret_cast<float2*>(p.part_rl)[r] = make_float2(m_used, l);
+      }
+    } else if (ok) {
       ptx::tc_fence_after();
       fold_last(tO, acc);
       // Normalise, round, stage in the (now free) Q tile buffer with the TMA
@@ -591,13 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int q_row0 = (2 * pair + t) * kBM + wq * 32;
+        const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;
         if (q_row0 < p.Sq) {
           int c1, c2;
-          tma_coords(p.layout, q_row0, head, c1, c2);
+          tma_coords(p.layout, q_row0, wk.head, c1, c2);
           for (int hf = 0; hf < 2; ++hf)
             ptx::tma_store_4d(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1, c2,
-                              batch);
+                              wk.batch);
           ptx::bulk_commit_group();
           ptx::bulk_wait_group_0();
         }

@@ -79,6 +79,43 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
              int rounding_mode, void* stream);
 
+/*
+ * Split-KV: the same operation with each query tile's key range cut into
+ * `num_splits` contiguous parts handled by different CTAs, for shapes with too
+ * few (batch, head, query-tile) units to fill the GPU (short queries against long
+ * keys). Each part writes an unnormalised fp32 partial result and its running max
+ * and row sum to `workspace`; a second kernel merges the parts in a fixed order,
+ * normalises and rounds to bf16 per mode into `out`. The numerics contract of
+ * attn_fwd holds; results are bit-identical from run to run for a given
+ * num_splits (but not bit-identical to other split counts: the fp32 sums run in
+ * another order). This is the first of the follow-on steps after the fused
+ * kernel; the pages' kernel processes each query tile's keys in one CTA.
+ *
+ *   num_splits       1 .. ceil(Sk / 128); 1 runs attn_fwd and needs no workspace
+ *   workspace        device, 16-byte aligned, at least
+ *                    attn_fwd_splitkv_workspace_bytes(...) bytes, owned by the
+ *                    caller, not overlapping q, k, v or out; its contents on
+ *                    entry do not matter and are overwritten
+ *   workspace_bytes  its size in bytes
+ * Other arguments as attn_fwd. Two kernels are launched on `stream`; calls that
+ * share a workspace must not overlap in time. Returns ATTN_OK or a status code
+ * (ATTN_ERR_INVALID_ARG for a bad split count or a missing / short workspace).
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, int layout,
+                     int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                     int rounding_mode, int num_splits, void* workspace, int64_t workspace_bytes,
+                     void* stream);
+
+/* Workspace bytes attn_fwd_splitkv needs (0 for num_splits == 1), or a negative
+ * status code for invalid sizes. Host only. */
+int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
+                                         int num_splits);
+
+/* A split count that fills the current device once (1 when the problem already
+ * has at least one query-tile pair per SM), keeping at least 4 key tiles per
+ * split and at most 64 splits. Negative status code for invalid sizes. */
+int attn_fwd_splitkv_num_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk);
+
 /* Static English text for a status code (never NULL). */
 const char* attn_status_str(int status);
 

@@ -89,6 +89,41 @@ def test_timeout_selftest_validation(lib):
     assert attn.attn_fwd_timeout_selftest_raw(*bad, 0, 10_000_000) == attn.ATTN_ERR_INVALID_ARG
 
 
+def _split(q=A, k=2 * A, v=3 * A, o=4 * A, B=1, H=2, Sq=256, Sk=1000, splits=2, ws=8 * A,
+           ws_bytes=1 << 24):
+    return attn.attn_fwd_splitkv_raw(q, k, v, o, 0, B, H, Sq, Sk, 128, 0.088, 0, splits, ws, ws_bytes, 0)
+
+
+def test_splitkv_workspace_bytes(lib):
+    assert attn.splitkv_workspace_bytes(1, 2, 256, 1000, 1) == 0
+    # splits x B x H x rows (padded to 256) x (128 + 2) fp32
+    assert attn.splitkv_workspace_bytes(1, 2, 256, 1000, 2) == 2 * 2 * 256 * 130 * 4
+    assert attn.splitkv_workspace_bytes(3, 1, 300, 1000, 8) == 8 * 3 * 512 * 130 * 4
+    for bad in [(1, 2, 256, 1000, 0), (1, 2, 256, 1000, 9), (0, 2, 256, 1000, 2)]:
+        with pytest.raises(attn.AttnError):
+            attn.splitkv_workspace_bytes(*bad)
+    assert attn.splitkv_num_splits(2, 16, 8192, 8192) == 1
+    assert 1 <= attn.splitkv_num_splits(1, 1, 100, 4096) <= 8
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(splits=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(splits=9), attn.ATTN_ERR_INVALID_ARG),          # 1000 keys = 8 tiles
+    (dict(ws=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws_bytes=1000), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws=8 * A + 4), attn.ATTN_ERR_MISALIGNED),
+    (dict(ws=4 * A + 256), attn.ATTN_ERR_ALIASING),       # overlaps out
+    (dict(ws=2 * A), attn.ATTN_ERR_ALIASING),             # overlaps k
+])
+def test_splitkv_validation(lib, kw, status):
+    assert _split(**kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
+def test_splitkv_valid_call_without_gpu_reports_no_device(lib):
+    assert _split() == attn.ATTN_ERR_NO_DEVICE
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
 def test_valid_call_without_gpu_reports_no_device(lib):
     assert _call() == attn.ATTN_ERR_NO_DEVICE
