@@ -27,6 +27,7 @@ ATTN_ERR_ARCH = -6
 ATTN_ERR_LAUNCH = -7
 ATTN_ERR_TIMEOUT = -8
 ATTN_ERR_TOO_LARGE = -9
+ATTN_ERR_SCRATCH = -10
 
 _lib = None
 
@@ -70,6 +71,11 @@ def load_library() -> ctypes.CDLL:
     lib.attn_fwd_splitkv_workspace_bytes.restype = i64
     lib.attn_fwd_splitkv_num_splits.argtypes = [i64, i64, i64, i64]
     lib.attn_fwd_splitkv_num_splits.restype = ctypes.c_int
+    lib.attn_fwd_splitkv_noalloc.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64,
+                                                                     i64, i64, ctypes.c_float,
+                                                                     ctypes.c_int, ctypes.c_int,
+                                                                     ctypes.c_void_p]
+    lib.attn_fwd_splitkv_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -103,6 +109,17 @@ def attn_fwd_splitkv_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layou
     return load_library().attn_fwd_splitkv(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq, Sk, d,
                                            ctypes.c_float(scale), rounding_mode, num_splits,
                                            workspace_ptr, workspace_bytes, stream)
+
+
+def attn_fwd_splitkv_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int,
+                                 B: int, H: int, Sq: int, Sk: int, d: int, scale: float,
+                                 rounding_mode: int, num_splits: int, stream: int) -> int:
+    """Direct call of ``attn_fwd_splitkv_noalloc``: split-KV whose workspace is the
+    library's fixed device scratch array, for callers that cannot allocate device
+    memory (see include/attn_fwd.h). Returns its status code."""
+    return load_library().attn_fwd_splitkv_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq,
+                                                   Sk, d, ctypes.c_float(scale), rounding_mode,
+                                                   num_splits, stream)
 
 
 def splitkv_workspace_bytes(B: int, H: int, Sq: int, Sk: int, num_splits: int, d: int = 128) -> int:
@@ -216,5 +233,5 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
 
 __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw",
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
-           "splitkv_num_splits", "status_str", "load_library",
+           "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

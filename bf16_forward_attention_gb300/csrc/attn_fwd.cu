@@ -139,6 +139,7 @@ const char* attn_status_str(int status) {
     case ATTN_ERR_LAUNCH: return "CUDA launch or tensor-map setup failed";
     case ATTN_ERR_TIMEOUT: return "a device-side wait timed out";
     case ATTN_ERR_TOO_LARGE: return "size beyond tensor-map or grid limits";
+    case ATTN_ERR_SCRATCH: return "split workspace needed exceeds the library's fixed 32 MiB device scratch";
     default: return "unknown status";
   }
 }
@@ -311,3 +312,53 @@ int attn_fwd_last_error(void) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation split-KV
+//
+// Some callers cannot allocate device memory when they need attention: a plugin
+// inside a framework whose own pool owns every device allocation, a serving loop
+// that must not call cudaMalloc / cudaFree after start-up (those calls can
+// synchronise the device and stall every stream), or a host with no allocator
+// beyond what this library brings. For them the split workspace lives in a fixed
+// array in the library's device memory. Every GPU that loads the library holds
+// these 32 MiB until the process exits.
+static constexpr int64_t kNoAllocScratchBytes = int64_t(32) << 20;
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices];  // device address of the scratch array, per device
+}  // namespace
+
+extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* out,
+                                        int layout, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                        int64_t d, float scale, int rounding_mode, int num_splits,
+                                        void* stream) {
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  const int64_t need = attn_fwd_splitkv_workspace_bytes(B, H, Sq, Sk, d, num_splits);
+  if (need < 0) return static_cast<int>(need);
+  if (need > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+  void* scratch = nullptr;
+  {
+    // Once per device, with that device current: the array's name is only a
+    // host-side stand-in, so the kernel is given the device address instead.
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_attn_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return ATTN_ERR_LAUNCH;
+      }
+      g_scratch_addr[dev] = ptr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
+                       kTimeoutNs, 0, num_splits, scratch, kNoAllocScratchBytes);
+}

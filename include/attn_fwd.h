@@ -51,7 +51,8 @@ enum {
   ATTN_ERR_ARCH = -6,        /* current device is not compute capability 10.3  */
   ATTN_ERR_LAUNCH = -7,      /* the CUDA launch (or tensor-map setup) failed   */
   ATTN_ERR_TIMEOUT = -8,     /* a bounded device-side wait expired             */
-  ATTN_ERR_TOO_LARGE = -9    /* a size beyond the tensor-map / grid limits     */
+  ATTN_ERR_TOO_LARGE = -9,   /* a size beyond the tensor-map / grid limits     */
+  ATTN_ERR_SCRATCH = -10     /* attn_fwd_splitkv_noalloc: workspace > 32 MiB   */
 };
 
 /*
@@ -115,6 +116,33 @@ int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64
  * has at least one query-tile pair per SM), keeping at least 4 key tiles per
  * split and at most 64 splits. Negative status code for invalid sizes. */
 int attn_fwd_splitkv_num_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk);
+
+/*
+ * attn_fwd_splitkv_noalloc - attn_fwd_splitkv for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this entry point. It exists because some
+ * callers cannot allocate device memory when they need attention: a plugin
+ * inside a framework whose own pool owns every device allocation, a serving loop
+ * that must not call cudaMalloc / cudaFree after start-up (those calls can
+ * synchronise the device and stall every stream), or a host with no allocator
+ * of its own. Here the split workspace is a fixed 32 MiB array in the library's
+ * device memory, held by every GPU that loads the library until the process
+ * exits; the call allocates nothing. The caller still passes q, k, v and out.
+ *
+ *   - Arguments and results as attn_fwd_splitkv, without the workspace.
+ *   - A problem whose split workspace (attn_fwd_splitkv_workspace_bytes) exceeds
+ *     32 MiB is rejected with ATTN_ERR_SCRATCH before anything is launched.
+ *   - The first call on a device looks up the array's device address for that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array, and each call overwrites the
+ *     part it uses before reading it (nothing has to start at zero). Calls that
+ *     overlap in time on the GPU, from any stream or thread, race on it: order
+ *     them on one stream or synchronise between them.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* out, int layout,
+                             int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                             int rounding_mode, int num_splits, void* stream);
 
 /* Static English text for a status code (never NULL). */
 const char* attn_status_str(int status);

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for st in range(0, -10, -1):
+    for st in range(0, -11, -1):
         s = attn.status_str(st)
         assert s and s != "unknown status", st
     assert attn.status_str(-1234) == "unknown status"
