@@ -225,10 +225,21 @@ def run_ours(args, w):
     outs = {m: torch.empty_like(q) for m in w.roundings}
     stream = torch.cuda.current_stream(dev)
     flops_call = float(w.flops)
+    splits, workspace = 1, None
+    if w.splitkv:
+        splits = attn.splitkv_num_splits(w.B, w.H, w.Sq, w.Sk)
+        workspace = torch.empty(max(16, attn.splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, splits)),
+                                dtype=torch.uint8, device=dev)
+
+    def call(qq, kk, vv, m, out=None):
+        if splits > 1:
+            return attn.attn_fwd_splitkv(qq, kk, vv, num_splits=splits, layout=w.layout,
+                                         rounding=m, out=out, workspace=workspace)
+        return attn.attn_fwd(qq, kk, vv, layout=w.layout, rounding=m, out=out)
 
     def step():
         for m in w.roundings:
-            attn.attn_fwd(q, k, v, layout=w.layout, rounding=m, out=outs[m])
+            call(q, k, v, m, outs[m])
 
     for _ in range(args.warmup):
         step()
@@ -253,7 +264,7 @@ def run_ours(args, w):
     for _ in range(args.steps):
         for m in w.roundings:
             ev[i][0].record(stream)
-            attn.attn_fwd(q, k, v, layout=w.layout, rounding=m, out=outs[m])
+            call(q, k, v, m, outs[m])
             ev[i][1].record(stream)
             i += 1
     t_end.record(stream)
@@ -281,8 +292,7 @@ def run_ours(args, w):
     def e2e_step():
         qd, kd, vd = (t.to(dev, non_blocking=True) for t in (qp, kp, vp))
         for m in w.roundings:
-            host_out[m].copy_(attn.attn_fwd(qd, kd, vd, layout=w.layout, rounding=m),
-                              non_blocking=True)
+            host_out[m].copy_(call(qd, kd, vd, m), non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -327,12 +337,13 @@ def run_ours(args, w):
                      "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else _recorded_traffic(w.name),
                      "peak_kind": f"{'sustained' if sustained else 'burst'} dense bf16 ({peak_src})",
-                     "kernel": "attn_fwd_kernel",
+                     "kernel": "attn_fwd_kernel" + (" + attn_splitkv_combine" if splits > 1 else ""),
                      "note": "achieved counts 4*B*H*Sq*Sk*d per launch; the kernel also runs the "
                              "P_lo*V product, 1.5x the counted tensor work"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": n_calls,
+        "gpu_launches": n_calls * (2 if splits > 1 else 1),
+        "splits": splits,
         "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
     }

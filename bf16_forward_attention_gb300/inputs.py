@@ -126,6 +126,7 @@ class Workload:
     specials: bool = False  # one NaN in Q and one +Inf in K per batch
     roundings: tuple = ("rtne",)
     seed: int = 20260001
+    splitkv: bool = False  # run with the key range split over CTAs
 
     @property
     def flops(self) -> int:
@@ -150,6 +151,9 @@ WORKLOADS = {
     "stress16381": Workload("stress16381", "bhsd", 4, 24, 16381, 16381, qk_std=8.0,
                             v_dist="uniform", specials=True, roundings=("rtz",),
                             seed=20260005),
+    # Follow-on workload for the split-KV path: few query rows against long keys.
+    "decode32k": Workload("decode32k", "bhsd", 1, 8, 256, 32768, roundings=("rtne",),
+                          seed=20260006, splitkv=True),
 }
 
 

@@ -27,6 +27,11 @@ Readings where the pages are silent (each is listed in the design notes):
     toward zero. Rounded once, from the fp64 value. bf16 subnormals are kept.
     Overflow: RTNE/RTNA -> +-Inf, RTZ -> +-max finite.
   * every NaN output is written as the one pattern 0x7FC0.
+  * causal (a follow-on step the pages name as missing): key j is visible to
+    query i iff j <= i + (Sk - Sq), the bottom-right alignment that makes the last
+    query see every key; hidden logits are -Inf, so a row that sees no key is NaN.
+  * grouped-query attention (also named as missing): Hq query heads share Hkv
+    key/value heads, query head h reads K/V head h // (Hq // Hkv).
 """
 from __future__ import annotations
 
@@ -64,7 +69,7 @@ def _ieee_matmul(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 
 
 def attention_rows_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
-                        rows=None) -> np.ndarray:
+                        rows=None, causal: bool = False) -> np.ndarray:
     """O rows of one head, in fp64.
 
     q: (Sq, d), k: (Sk, d), v: (Sk, d), float64. rows: indices into Sq (default all).
@@ -75,12 +80,16 @@ def attention_rows_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: floa
       l_i  = sum_j p_ij
       O_ic = (sum_j p_ij v_jc) / l_i
     The matrix products are library primitives; nothing is blocked or fused across
-    the key axis.
+    the key axis. With causal, s_ij = -Inf for j > i + (Sk - Sq).
     """
     scale_d = float(np.float32(scale))
-    if rows is not None:
-        q = q[np.asarray(rows)]
+    Sq_all, Sk = q.shape[0], k.shape[0]
+    idx = np.arange(Sq_all) if rows is None else np.asarray(rows)
+    q = q[idx]
     s = _ieee_matmul(q, k.T) * scale_d
+    if causal:
+        hidden = np.arange(Sk)[None, :] > (idx[:, None] + (Sk - Sq_all))
+        s = np.where(hidden, -np.inf, s)
     with np.errstate(invalid="ignore", over="ignore"):
         m = np.max(s, axis=1, keepdims=True)  # np.max propagates NaN
         p = np.exp(s - m)
@@ -90,22 +99,27 @@ def attention_rows_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: floa
 
 
 def attention_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
-                   layout: str = "bhsd") -> np.ndarray:
+                   layout: str = "bhsd", causal: bool = False) -> np.ndarray:
     """Full attention for (B, H, S, d) or (B, S, H, d) float64 arrays.
 
     Returns O in the input layout (the pages' kernel reads either layout without a
     transpose; the output keeps the layout of the inputs). Rows are independent,
-    so they are processed in groups of rows to bound memory.
+    so they are processed in groups of rows to bound memory. K and V may have
+    fewer heads than Q (grouped-query attention, Hq a multiple of Hkv).
     """
     qb, kb, vb = to_bhsd(q, layout), to_bhsd(k, layout), to_bhsd(v, layout)
     B, H, Sq, d = qb.shape
+    Hkv = kb.shape[1]
+    if H % Hkv:
+        raise ValueError("query heads must be a multiple of key/value heads")
+    group = H // Hkv
     out = np.empty((B, H, Sq, d), dtype=np.float64)
     for b in range(B):
         for h in range(H):
-            kh, vh = kb[b, h], vb[b, h]
+            kh, vh = kb[b, h // group], vb[b, h // group]
             for r0 in range(0, Sq, _ROW_BLOCK):
                 rows = np.arange(r0, min(Sq, r0 + _ROW_BLOCK))
-                out[b, h, rows] = attention_rows_fp64(qb[b, h], kh, vh, scale, rows)
+                out[b, h, rows] = attention_rows_fp64(qb[b, h], kh, vh, scale, rows, causal)
     if layout == "bshd":
         out = np.ascontiguousarray(np.swapaxes(out, 1, 2))
     return out

@@ -174,7 +174,7 @@ def test_generator_is_deterministic_and_shaped():
 # --- planted mistakes: each must be caught by a pin above -----------------------
 
 def _mutant(kind):
-    def rows(q, k, v, scale, rows=None):
+    def rows(q, k, v, scale, rows=None, causal=False):
         scale_d = float(np.float32(scale))
         if rows is not None:
             q = q[np.asarray(rows)]
@@ -207,3 +207,47 @@ def test_planted_mistakes_are_caught(kind, monkeypatch):
     got = oa.attention_fp64(q, k, v, scale)
     want = _sdpa(q, k, v, float(np.float32(scale)))
     assert not np.allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+# --- follow-on steps: causal mask (bottom-right aligned) and grouped-query heads --
+
+def _sdpa_mask(q, k, v, scale, mask):
+    qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(a)) for a in (q, k, v))
+    return torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=torch.from_numpy(mask), scale=scale).numpy()
+
+
+@pytest.mark.parametrize("Sq,Sk", [(7, 7), (5, 12), (130, 300)])
+def test_causal_matches_sdpa_with_explicit_mask(Sq, Sk):
+    q, k, v = _rand((1, 2, Sq, 128), 40), _rand((1, 2, Sk, 128), 41), _rand((1, 2, Sk, 128), 42)
+    scale = inputs.default_scale()
+    allowed = np.arange(Sk)[None, :] <= np.arange(Sq)[:, None] + (Sk - Sq)
+    got = attention_fp64(q, k, v, scale, causal=True)
+    want = _sdpa_mask(q, k, v, float(np.float32(scale)), allowed)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_causal_closed_forms():
+    q, k, v = _rand((1, 1, 6, 128), 43), _rand((1, 1, 6, 128), 44), _rand((1, 1, 6, 128), 45)
+    o = attention_fp64(q, k, v, 0.1, causal=True)
+    assert (o[0, 0, 0] == v[0, 0, 0]).all()           # first query sees only key 0
+    full = attention_fp64(q, k, v, 0.1)
+    np.testing.assert_allclose(o[0, 0, -1], full[0, 0, -1], rtol=1e-14)  # last sees all
+    # more queries than keys: the first Sq - Sk rows see no key and are NaN
+    o = attention_fp64(_rand((1, 1, 9, 128), 46), k[:, :, :4], v[:, :, :4], 0.1, causal=True)
+    assert np.isnan(o[0, 0, :5]).all() and np.isfinite(o[0, 0, 5:]).all()
+    assert (o[0, 0, 5] == v[0, 0, 0]).all()
+
+
+def test_gqa_equals_repeated_heads_and_sdpa():
+    q = _rand((2, 6, 11, 128), 47)
+    k, v = _rand((2, 2, 13, 128), 48), _rand((2, 2, 13, 128), 49)
+    got = attention_fp64(q, k, v, 0.09)
+    rep = attention_fp64(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1), 0.09)
+    assert (got == rep).all()
+    qt, kt, vt = (torch.from_numpy(a) for a in (q, k, v))
+    want = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=float(np.float32(0.09)),
+                                                            enable_gqa=True).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+    with pytest.raises(ValueError):
+        attention_fp64(q, k[:, :1].repeat(4, axis=1), v[:, :1].repeat(4, axis=1), 0.1)
