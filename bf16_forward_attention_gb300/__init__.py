@@ -28,6 +28,7 @@ ATTN_ERR_LAUNCH = -7
 ATTN_ERR_TIMEOUT = -8
 ATTN_ERR_TOO_LARGE = -9
 ATTN_ERR_SCRATCH = -10
+ATTN_FLAG_CAUSAL = 1
 
 _lib = None
 
@@ -76,6 +77,10 @@ def load_library() -> ctypes.CDLL:
                                                                      ctypes.c_int, ctypes.c_int,
                                                                      ctypes.c_void_p]
     lib.attn_fwd_splitkv_noalloc.restype = ctypes.c_int
+    lib.attn_fwd_ex.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64, i64, i64, i64,
+                                                        ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                        ctypes.c_void_p]
+    lib.attn_fwd_ex.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -177,6 +182,45 @@ def attn_fwd_splitkv(q, k, v, *, num_splits: int | None = None, layout: str = "b
     return out
 
 
+def attn_fwd_ex_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, B: int, Hq: int,
+                    Hkv: int, Sq: int, Sk: int, d: int, scale: float, rounding_mode: int,
+                    flags: int, stream: int) -> int:
+    """Direct call of ``attn_fwd_ex`` (grouped-query heads, causal flag)."""
+    return load_library().attn_fwd_ex(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, Hq, Hkv, Sq, Sk, d,
+                                      ctypes.c_float(scale), rounding_mode, flags, stream)
+
+
+def attn_fwd_ex(q, k, v, *, causal: bool = False, layout: str = "bhsd",
+                scale: float | None = None, rounding: str = "rtne", out=None):
+    """attn_fwd with grouped-query heads (k, v may have fewer heads than q, a divisor
+    of q's) and an optional causal mask aligned at the bottom right."""
+    import torch
+
+    if layout not in LAYOUTS or rounding not in ROUNDINGS:
+        raise ValueError("unknown layout or rounding mode")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, Hq, Sq, D = _dims(q, layout)
+    Bk, Hkv, Sk, Dk = _dims(k, layout)
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             LAYOUTS[layout], B, Hq, Hkv, Sq, Sk, D, float(scale),
+                             ROUNDINGS[rounding], ATTN_FLAG_CAUSAL if causal else 0, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, status_str(st))
+    return out
+
+
 def attn_fwd_last_error() -> int:
     return load_library().attn_fwd_last_error()
 
@@ -233,5 +277,5 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
 
 __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw",
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
-           "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "status_str", "load_library",
+           "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

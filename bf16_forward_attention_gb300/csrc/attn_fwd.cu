@@ -56,21 +56,24 @@ int device_ready(int dev) {
     g_dev_state[dev] = ATTN_ERR_ARCH;
     return ATTN_ERR_ARCH;
   }
-  if (cudaFuncSetAttribute(attn::attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           attn::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(attn::attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           attn::kSmemBytes) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_LAUNCH;
+  // Every variant of the fused kernel (whole key range / split; causal).
+  const void* variants[] = {reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false>),
+                            reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false>),
+                            reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true>)};
+  for (const void* fn : variants) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
   }
   // The kernel's warpgroups re-split the registers a CTA is launched with
   // (setmaxnreg); the split only adds up if each thread starts with exactly
   // kLaunchRegs. A build with another count would make setmaxnreg.inc wait
   // forever, so it is refused here.
-  for (int i = 0; i < 2; ++i) {
+  for (const void* fn : variants) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, i ? attn::attn_fwd_kernel<true> : attn::attn_fwd_kernel<false>) !=
-        cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
@@ -153,11 +156,13 @@ namespace {
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
                   int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
                   void* stream, unsigned long long timeout_ns, int withhold_s0, int n_splits,
-                  void* workspace, int64_t workspace_bytes) {
+                  void* workspace, int64_t workspace_bytes, int64_t Hkv = 0, int causal = 0) {
+  if (Hkv == 0) Hkv = H;
   // ---- host-side validation (nothing is launched on failure)
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || Hkv < 1 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal && n_splits != 1) return ATTN_ERR_UNSUPPORTED;
   if (d != 128) return ATTN_ERR_UNSUPPORTED;
   if (layout != ATTN_LAYOUT_BHSD && layout != ATTN_LAYOUT_BSHD) return ATTN_ERR_UNSUPPORTED;
   if (rounding_mode < ATTN_ROUND_RTNE || rounding_mode > ATTN_ROUND_RTZ) return ATTN_ERR_UNSUPPORTED;
@@ -173,7 +178,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   const uintptr_t ormask = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                            reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
   if (ormask & 15u) return ATTN_ERR_MISALIGNED;
-  const uint64_t bytes_q = uint64_t(B) * H * Sq * 256, bytes_kv = uint64_t(B) * H * Sk * 256;
+  const uint64_t bytes_q = uint64_t(B) * H * Sq * 256, bytes_kv = uint64_t(B) * Hkv * Sk * 256;
   if (overlaps(out, bytes_q, q, bytes_q) || overlaps(out, bytes_q, k, bytes_kv) ||
       overlaps(out, bytes_q, v, bytes_kv))
     return ATTN_ERR_ALIASING;
@@ -196,8 +201,8 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   if (st != ATTN_OK) return st;
 
   CUtensorMap tq, tk, tv, to;
-  if (!make_map(&tq, q, layout, B, H, Sq, attn::kBM) || !make_map(&tk, k, layout, B, H, Sk, attn::kBN) ||
-      !make_map(&tv, v, layout, B, H, Sk, attn::kBN) || !make_map(&to, out, layout, B, H, Sq, 32))
+  if (!make_map(&tq, q, layout, B, H, Sq, attn::kBM) || !make_map(&tk, k, layout, B, Hkv, Sk, attn::kBN) ||
+      !make_map(&tv, v, layout, B, Hkv, Sk, attn::kBN) || !make_map(&to, out, layout, B, H, Sq, 32))
     return ATTN_ERR_LAUNCH;
 
   attn::Params p;
@@ -218,13 +223,18 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.c = scale * 1.4426950408889634f;
   p.timeout_ns = timeout_ns;
   p.withhold_s0 = withhold_s0;
+  p.group = static_cast<int>(H / Hkv);
+  p.causal = causal ? 1 : 0;
+  p.causal_off = static_cast<int>(Sk - Sq);
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
-  if (n_splits == 1) {
-    attn::attn_fwd_kernel<false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+  if (causal) {
+    attn::attn_fwd_kernel<false, true><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+  } else if (n_splits == 1) {
+    attn::attn_fwd_kernel<false, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
   } else {
-    attn::attn_fwd_kernel<true><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+    attn::attn_fwd_kernel<true, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
     attn::CombineParams cp;
     cp.part_o = p.part_o;
     cp.part_rl = p.part_rl;
@@ -252,6 +262,15 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
              void* stream) {
   return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
                        kTimeoutNs, 0, 1, nullptr, 0);
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
+                int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                int rounding_mode, int flags, void* stream) {
+  if (flags & ~ATTN_FLAG_CAUSAL) return ATTN_ERR_UNSUPPORTED;
+  if (Hkv < 1) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, out, layout, B, Hq, Sq, Sk, d, scale, rounding_mode, stream,
+                       kTimeoutNs, 0, 1, nullptr, 0, Hkv, (flags & ATTN_FLAG_CAUSAL) ? 1 : 0);
 }
 
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,

@@ -102,6 +102,9 @@ struct Params {
   float c;       // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_s0;  // self-test of the timeout path: never signal query tile 0's first S
+  int group;        // query heads per key/value head (grouped-query attention)
+  int causal;       // 1: key j visible to query i iff j <= i + causal_off
+  int causal_off;   // Sk - Sq
 };
 
 // Bit 0: some wait timed out.
@@ -366,7 +369,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // head are adjacent (so K/V of a head stay in L2). Recomputed by each role where
 // it is needed, rather than kept live across the softmax loop.
 struct Work {
-  int split, pair, bh, head, batch;
+  int split, pair, bh, head, kv_head, batch;
   int tile0, n_kv;  // key tiles [tile0, tile0 + n_kv)
   bool has_tail;    // this split holds the ragged last key tile
 };
@@ -376,20 +379,31 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   w.split = blockIdx.x % p.n_splits;
   const int item = blockIdx.x / p.n_splits;
   w.pair = item % p.n_qpairs;
+  if (p.causal) w.pair = p.n_qpairs - 1 - w.pair;  // longest key ranges first
   w.bh = item / p.n_qpairs;
   w.head = w.bh % p.H;
+  w.kv_head = w.head / p.group;
   w.batch = w.bh / p.H;
   const int base = p.kv_tiles / p.n_splits, rem = p.kv_tiles % p.n_splits;
   w.tile0 = w.split * base + (w.split < rem ? w.split : rem);
   w.n_kv = base + (w.split < rem ? 1 : 0);
+  if (p.causal) {
+    // Key tiles up to the diagonal of the pair's last row (at least one, so that
+    // a row with no visible key still runs and comes out NaN).
+    const int last_row = min(p.Sq, 2 * kBM * (w.pair + 1)) - 1;
+    const int visible = last_row + p.causal_off + 1;
+    const int tiles = visible <= 0 ? 1 : (visible + kBN - 1) / kBN;
+    w.n_kv = min(tiles, p.kv_tiles);
+  }
   w.has_tail = w.tile0 + w.n_kv == p.kv_tiles && p.kv_tail < kBN;
   return w;
 }
 
 // kPartial: the CTA covers one split of the key range and writes its fp32 partial
 // result to the workspace (combined by attn_splitkv_combine); otherwise the CTA
-// covers all keys and stores bf16 output.
-template <bool kPartial>
+// covers all keys and stores bf16 output. kCausal: the causal mask (p.causal
+// must agree); compiled separately so that the other variants carry none of it.
+template <bool kPartial, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -448,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const Work wk = work_of(p);
         const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
+        const int kv_head = wk.kv_head;
         int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
         int c1, c2;
         ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
@@ -462,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t parity = ((it / kStages) & 1) ^ 1;
           if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
           const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-          tma_coords(p.layout, (tile0 + (it >> 1)) * kBN, head, c1, c2);
+          tma_coords(p.layout, (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
           ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
             ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
@@ -558,7 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
     bool ok = true;
-    const int n_kv = work_of(p).n_kv;  // key tiles of this CTA
+    int n_kv, row_lim;
+    {
+      const Work wk = work_of(p);
+      n_kv = wk.n_kv;  // key tiles of this CTA
+      // Causal: number of keys this row sees, counted from key 0 (capped at Sk,
+      // which also hides the ragged tail from the padding rows past Sq).
+      row_lim = kCausal ? min((2 * wk.pair + t) * kBM + row + p.causal_off + 1, p.Sk) : 0;
+    }
 
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = warp_wait(bar(kBarSFull + t), j & 1, abort_flag, p.timeout_ns))) break;
@@ -568,21 +590,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // register allocation of this loop free of spills.
       const bool last = (j == n_kv - 1) && (p.kv_tail < kBN) &&
                         (!kPartial || static_cast<int>(blockIdx.x % p.n_splits) == p.n_splits - 1);
+      // Masked tile: the ragged last tile; with the causal mask every tile, each
+      // row hiding the keys beyond its own limit (a tile it fully sees loses
+      // nothing). One path for all tiles keeps the loop's registers spill-free.
+      const bool masked = kCausal ? true : last;
+      const int valid = kCausal ? row_lim - kBN * j : p.kv_tail;
       // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
       // holds exactly that tile: the MMA that wrote S_j was issued after
       // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
       float ext;
       if (pos) {
         if (j == 0) {
-          ext = last ? fold_and_max<true, false>(tS, tO, acc, p.kv_tail)
-                     : fold_and_max<false, false>(tS, tO, acc, kBN);
+          ext = masked ? fold_and_max<true, false>(tS, tO, acc, valid)
+                       : fold_and_max<false, false>(tS, tO, acc, kBN);
         } else {
-          ext = last ? fold_and_max<true, true>(tS, tO, acc, p.kv_tail)
-                     : fold_and_max<false, true>(tS, tO, acc, kBN);
+          ext = masked ? fold_and_max<true, true>(tS, tO, acc, valid)
+                       : fold_and_max<false, true>(tS, tO, acc, kBN);
         }
       } else {
-        ext = last ? fold_and_min<true>(tS, tO, acc, p.kv_tail, j > 0)
-                   : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
+        ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
+                     : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
       }
       const float m_tile = ext * c;
       const bool need = m_tile > m_used + kTau;  // false for NaN
@@ -593,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_tile;
       }
       const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
-      l += last ? tile_exp<true>(tS, p.kv_tail, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
+      l += masked ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kBarPFull + t));

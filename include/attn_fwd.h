@@ -80,6 +80,28 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
              int rounding_mode, void* stream);
 
+/* Flags of attn_fwd_ex. */
+enum { ATTN_FLAG_CAUSAL = 1 };
+
+/*
+ * attn_fwd_ex - attn_fwd with two of the follow-on steps the pages list as
+ * missing from their kernel (tilnote.io note, performance section; snilld.dk,
+ * "Hvad er udgivet"): grouped-query attention and a causal mask.
+ *
+ *   Hq, Hkv  query heads and key/value heads; Hq must be a multiple of Hkv, and
+ *            query head h reads key/value head h / (Hq / Hkv). q and out have Hq
+ *            heads, k and v have Hkv heads, all in `layout`.
+ *   flags    0 or ATTN_FLAG_CAUSAL. Causal: key j is visible to query i iff
+ *            j <= i + (Sk - Sq) (aligned at the bottom right, so the last query
+ *            sees every key); hidden logits are -Inf, and a query that sees no
+ *            key (possible when Sq > Sk) comes out NaN. Key tiles that no row of
+ *            a query tile can see are skipped.
+ * Other arguments, ownership, errors and the numerics contract as attn_fwd.
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
+                int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                int rounding_mode, int flags, void* stream);
+
 /*
  * Split-KV: the same operation with each query tile's key range cut into
  * `num_splits` contiguous parts handled by different CTAs, for shapes with too

@@ -6,6 +6,12 @@ section "Numerik samlet eet sted", re-targeted at the exact fp64 result):
   * at least 99.9% of finite elements are within 1 bf16 ULP of the oracle's
     rounding (same mode) of the exact value;
   * max |err| against the exact fp64 value <= 8e-3 for unit-normal inputs.
+
+Where an output's magnitude reaches 2 (causal rows that see only a few keys),
+one bf16 ULP exceeds 8e-3 and the correctly rounded RTZ value itself can miss
+the absolute bound. There the bound applies to the kernel's error beyond the one
+the rounding mode forces: |gpu - exact| - |oracle - exact| <= 8e-3
+("max_excess_err").
 """
 from __future__ import annotations
 
@@ -35,6 +41,7 @@ def compare(gpu_bits: np.ndarray, exact: np.ndarray, mode: str) -> dict:
     d = ulp_distance(gpu_bits[fin], want[fin]) if fin.any() else np.zeros(0, np.int64)
     g = bf16_bits_to_f64(gpu_bits[fin])
     err = np.abs(g - exact[fin]) if fin.any() else np.zeros(0)
+    forced = np.abs(bf16_bits_to_f64(want[fin]) - exact[fin]) if fin.any() else np.zeros(0)
     return {
         "n": int(gpu_bits.size),
         "n_nonfinite": int(nf_w.sum()),
@@ -43,13 +50,16 @@ def compare(gpu_bits: np.ndarray, exact: np.ndarray, mode: str) -> dict:
         "within_1ulp": float((d <= 1).mean()) if d.size else 1.0,
         "max_ulp": int(d.max()) if d.size else 0,
         "max_abs_err": float(err.max()) if err.size else 0.0,
+        "max_excess_err": float((err - forced).max()) if err.size else 0.0,
         "exact_match": float((d == 0).mean()) if d.size else 1.0,
     }
 
 
-def assert_parity(stats: dict, max_abs_err: float | None = MAX_ABS_ERR):
+def assert_parity(stats: dict, max_abs_err: float | None = MAX_ABS_ERR, excess: bool = False):
+    """excess=True applies the absolute bound to max_excess_err (outputs that can
+    reach magnitude 2) instead of max_abs_err."""
     assert stats["nonfinite_positions_match"], stats
     assert stats["nonfinite_bits_match"], stats
     assert stats["within_1ulp"] >= ULP_FRACTION, stats
     if max_abs_err is not None:
-        assert stats["max_abs_err"] <= max_abs_err, stats
+        assert stats["max_excess_err" if excess else "max_abs_err"] <= max_abs_err, stats

@@ -124,6 +124,22 @@ def test_splitkv_valid_call_without_gpu_reports_no_device(lib):
     assert _split() == attn.ATTN_ERR_NO_DEVICE
 
 
+@pytest.mark.parametrize("Hq,Hkv,flags,status", [
+    (8, 3, 0, attn.ATTN_ERR_INVALID_ARG),     # Hq not a multiple of Hkv
+    (8, 0, 0, attn.ATTN_ERR_INVALID_ARG),
+    (8, 2, 2, attn.ATTN_ERR_UNSUPPORTED),     # unknown flag
+])
+def test_ex_validation(lib, Hq, Hkv, flags, status):
+    assert attn.attn_fwd_ex_raw(A, 2 * A, 3 * A, 4 * A, 0, 1, Hq, Hkv, 256, 256, 128, 0.088, 0,
+                                flags, 0) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
+def test_ex_valid_call_without_gpu_reports_no_device(lib):
+    assert attn.attn_fwd_ex_raw(A, 2 * A, 3 * A, 4 * A, 1, 1, 8, 2, 256, 300, 128, 0.088, 0,
+                                attn.ATTN_FLAG_CAUSAL, 0) == attn.ATTN_ERR_NO_DEVICE
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
 def test_valid_call_without_gpu_reports_no_device(lib):
     assert _call() == attn.ATTN_ERR_NO_DEVICE
