@@ -1,7 +1,7 @@
 """Benchmark: bf16 forward attention on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload self8k|cross4k32k|long128k|stress16381|tiny]
+                    [--workload self8k|cross4k32k|long128k|stress16381|tiny|decode32k|causal8k|gqa8k]
 
 Workload (default): self-attention, BSHD, B=2, H=16, Sq=Sk=8192, d=128, bf16
 Q/K/V ~ N(0,1) from a fixed seed, scale 1/sqrt(128). One step = one call of the
@@ -148,28 +148,39 @@ def _cpu_sample(w, q, k, v, budget_s: float):
 
     qb, kb, vb = (to_bhsd(t.view(torch.int16).numpy(), w.layout) for t in (q, k, v))
     scale = inputs.default_scale()
-    rows_done, t_used, i = 0, 0.0, 0
+    rows_done, pairs, t_used, i = 0, 0, 0.0, 0
     block = 256
+    group = w.H // w.kv_heads
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     while t_used < budget_s:
         b, h = heads[i % len(heads)]
         r0 = ((i // len(heads)) * block) % w.Sq
         rows = np.arange(r0, min(w.Sq, r0 + block))
-        kh, vh, qh = bf16_bits_to_f64(kb[b, h]), bf16_bits_to_f64(vb[b, h]), bf16_bits_to_f64(qb[b, h])
+        kh, vh = bf16_bits_to_f64(kb[b, h // group]), bf16_bits_to_f64(vb[b, h // group])
+        qh = bf16_bits_to_f64(qb[b, h])
         t0 = time.perf_counter()
-        attention_rows_fp64(qh, kh, vh, scale, rows)
+        attention_rows_fp64(qh, kh, vh, scale, rows, causal=w.causal)
         t_used += time.perf_counter() - t0
         rows_done += rows.size
+        pairs += (int(np.clip(rows + (w.Sk - w.Sq) + 1, 0, w.Sk).sum()) if w.causal
+                  else rows.size * w.Sk)
         i += 1
-    return 4.0 * rows_done * w.Sk * w.D, t_used, rows_done
+    return 4.0 * pairs * w.D, t_used, rows_done
+
+
+def _keys_seen(w):
+    return f"its visible keys of {w.Sk} (causal)" if w.causal else f"all {w.Sk} keys"
 
 
 def _config(w, world):
     big = 3 * 2 * w.B * w.H * max(w.Sq, w.Sk) * w.D > L2_BYTES
     return {"workload": f"{w.name}: {'self' if w.Sq == w.Sk else 'cross'}-attention fwd, "
                         f"{w.layout.upper()}, B={w.B}, H={w.H}, Sq={w.Sq}, Sk={w.Sk}, d={w.D}, "
-                        f"rounding {'/'.join(m.upper() for m in w.roundings)}",
+                        + (f"{w.kv_heads} key/value heads, " if w.kv_heads != w.H else "")
+                        + ("causal mask, " if w.causal else "")
+                        + f"rounding {'/'.join(m.upper() for m in w.roundings)}",
             "layout": w.layout, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "d": w.D,
+            "H_kv": w.kv_heads, "causal": w.causal,
             "roundings": list(w.roundings), "calls_per_step": len(w.roundings),
             "qk_dist": f"N(0,{w.qk_std:g}^2)", "v_dist": "N(0,1)" if w.v_dist == "normal" else "U(-1,1)",
             "specials": w.specials, "seed": w.seed,
@@ -198,7 +209,7 @@ def run_reference(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
-                         "sample": f"{rows} query rows of the workload, each against all {w.Sk} keys "
+                         "sample": f"{rows} query rows of the workload, each against {_keys_seen(w)} "
                                    f"(~{args.ref_step_seconds:g} s of fp64 CPU work per step)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -235,6 +246,9 @@ def run_ours(args, w):
         if splits > 1:
             return attn.attn_fwd_splitkv(qq, kk, vv, num_splits=splits, layout=w.layout,
                                          rounding=m, out=out, workspace=workspace)
+        if w.causal or w.kv_heads != w.H:
+            return attn.attn_fwd_ex(qq, kk, vv, causal=w.causal, layout=w.layout, rounding=m,
+                                    out=out)
         return attn.attn_fwd(qq, kk, vv, layout=w.layout, rounding=m, out=out)
 
     def step():
@@ -321,7 +335,7 @@ def run_ours(args, w):
     if not args.no_cpu_baseline and world == 1:
         f, t, rows = _cpu_sample(w, q_h, k_h, v_h, budget_s=args.cpu_seconds)
         cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
-               "sample": f"{rows} query rows of the workload, each against all {w.Sk} keys "
+               "sample": f"{rows} query rows of the workload, each against {_keys_seen(w)} "
                          f"({t:.1f} s of fp64 CPU work)"}
 
     line = {
@@ -338,8 +352,11 @@ def run_ours(args, w):
                      "traffic": args.traffic if args.traffic is not None else _recorded_traffic(w.name),
                      "peak_kind": f"{'sustained' if sustained else 'burst'} dense bf16 ({peak_src})",
                      "kernel": "attn_fwd_kernel" + (" + attn_splitkv_combine" if splits > 1 else ""),
-                     "note": "achieved counts 4*B*H*Sq*Sk*d per launch; the kernel also runs the "
-                             "P_lo*V product, 1.5x the counted tensor work"},
+                     "note": ("achieved counts 4*d per visible (query, key) pair and head "
+                              f"({w.visible_pairs} pairs per head under the causal mask) per launch"
+                              if w.causal else "achieved counts 4*B*H*Sq*Sk*d per launch")
+                             + "; the kernel also runs the P_lo*V product, 1.5x the counted tensor "
+                               "work"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": n_calls * (2 if splits > 1 else 1),

@@ -214,12 +214,22 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
 // (column 2i in the low half of pair i), updated with packed f32x2 arithmetic.
 using Row = uint64_t[kD / 2];
 
+// How a key tile is masked: not at all; per element (the ragged last tile); or,
+// in pass A only, per element in the 16-column chunks that reach past the warp's
+// least limit, writing the hidden logits back to TMEM as -Inf (the causal mask,
+// whose limits rise row by row; pass B then needs no mask when c > 0).
+enum MaskKind : int { kNoMask = 0, kElemMask = 1, kChunkMask = 2 };
+
 // Pass A over one key tile. Folds the previous key tile's products (TMEM O)
 // into the register row when kFold, and returns the row max of S (NaN if any
-// element is NaN). Columns >= valid (the key tail) are skipped when kMasked.
-// Both 16-column loads of a chunk are issued before one wait.
-template <bool kMasked, bool kFold>
-__device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, Row& acc, int valid) {
+// element is NaN). Columns >= valid are skipped unless kMask is kNoMask; with
+// kChunkMask, vmin is the least `valid` over the warp's lanes, so a chunk wholly
+// below it needs no test (the branch on it is uniform over the warp), and a
+// chunk that does is written back with its hidden columns set to -Inf. Both
+// 16-column loads of a chunk are issued before one wait.
+template <int kMask, bool kFold>
+__device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, Row& acc, int valid,
+                                              int vmin) {
   const float neg_inf = -__int_as_float(0x7F800000);
   float e0 = neg_inf, e1 = neg_inf;
 #pragma unroll
@@ -229,11 +239,14 @@ __device__ __forceinline__ float fold_and_max(uint32_t tS, uint32_t tO, Row& acc
     if (kFold) ptx::tmem_ld16_nowait(tO + 16 * ch, o);
     ptx::tmem_wait_ld16(r);
     if (kFold) ptx::reg_fence16(o);
+    if (kMask == kChunkMask)
+      ptx::mask16_store_uniform(r, valid - 16 * ch, 16 * ch + 16 <= vmin,
+                                __float_as_uint(neg_inf), tS + 16 * ch);
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
       float s0 = __uint_as_float(r[i]), s1 = __uint_as_float(r[i + 1]);
       float s2 = __uint_as_float(r[i + 2]), s3 = __uint_as_float(r[i + 3]);
-      if (kMasked) {
+      if (kMask == kElemMask) {
         if (16 * ch + i >= valid) s0 = neg_inf;
         if (16 * ch + i + 1 >= valid) s1 = neg_inf;
         if (16 * ch + i + 2 >= valid) s2 = neg_inf;
@@ -366,28 +379,37 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 // The CTA's share of the work: (batch, head, query-tile pair, key split) and the
 // split's key tiles. Splits of one pair are adjacent in the grid, pairs of one
-// head are adjacent (so K/V of a head stay in L2). Recomputed by each role where
-// it is needed, rather than kept live across the softmax loop.
+// head are adjacent (so K/V of a head stay in L2); under the causal mask the
+// pairs go longest first over all heads instead, which balances the SMs' loads
+// (the blocks running at one time still share each head's K/V through L2).
+// Recomputed by each role where it is needed, rather than kept live across the
+// softmax loop.
 struct Work {
   int split, pair, bh, head, kv_head, batch;
   int tile0, n_kv;  // key tiles [tile0, tile0 + n_kv)
   bool has_tail;    // this split holds the ragged last key tile
 };
 
+template <bool kCausal>
 __device__ __forceinline__ Work work_of(const Params& p) {
   Work w;
   w.split = blockIdx.x % p.n_splits;
   const int item = blockIdx.x / p.n_splits;
-  w.pair = item % p.n_qpairs;
-  if (p.causal) w.pair = p.n_qpairs - 1 - w.pair;  // longest key ranges first
-  w.bh = item / p.n_qpairs;
+  if (kCausal) {
+    // Longest key ranges first over the whole grid (blocks start in index order).
+    w.pair = p.n_qpairs - 1 - item / p.BH;
+    w.bh = item % p.BH;
+  } else {
+    w.pair = item % p.n_qpairs;
+    w.bh = item / p.n_qpairs;
+  }
   w.head = w.bh % p.H;
   w.kv_head = w.head / p.group;
   w.batch = w.bh / p.H;
   const int base = p.kv_tiles / p.n_splits, rem = p.kv_tiles % p.n_splits;
   w.tile0 = w.split * base + (w.split < rem ? w.split : rem);
   w.n_kv = base + (w.split < rem ? 1 : 0);
-  if (p.causal) {
+  if (kCausal) {
     // Key tiles up to the diagonal of the pair's last row (at least one, so that
     // a row with no visible key still runs and comes out NaN).
     const int last_row = min(p.Sq, 2 * kBM * (w.pair + 1)) - 1;
@@ -460,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        const Work wk = work_of(p);
+        const Work wk = work_of<kCausal>(p);
         const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
         const int kv_head = wk.kv_head;
         int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
@@ -497,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        const int n_kv = work_of(p).n_kv;
+        const int n_kv = work_of<kCausal>(p).n_kv;
         bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
         ptx::tc_fence_after();
         auto ring_wait = [&](int it) -> bool {
@@ -575,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int n_kv, row_lim;
     {
-      const Work wk = work_of(p);
+      const Work wk = work_of<kCausal>(p);
       n_kv = wk.n_kv;  // key tiles of this CTA
       // Causal: number of keys this row sees, counted from key 0 (capped at Sk,
       // which also hides the ragged tail from the padding rows past Sq).
@@ -594,18 +616,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row hiding the keys beyond its own limit (a tile it fully sees loses
       // nothing). One path for all tiles keeps the loop's registers spill-free.
       const bool masked = kCausal ? true : last;
+      constexpr int kM = kCausal ? kChunkMask : kElemMask;
       const int valid = kCausal ? row_lim - kBN * j : p.kv_tail;
+      // Least `valid` over the warp (lane 0 has the warp's first row).
+      const int vmin = kCausal ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
       // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
       // holds exactly that tile: the MMA that wrote S_j was issued after
       // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
       float ext;
       if (pos) {
         if (j == 0) {
-          ext = masked ? fold_and_max<true, false>(tS, tO, acc, valid)
-                       : fold_and_max<false, false>(tS, tO, acc, kBN);
+          ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                       : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
         } else {
-          ext = masked ? fold_and_max<true, true>(tS, tO, acc, valid)
-                       : fold_and_max<false, true>(tS, tO, acc, kBN);
+          ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                       : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
         }
       } else {
         ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
@@ -620,14 +645,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_tile;
       }
       const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
-      l += masked ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
+      // Causal, c > 0: pass A left -Inf in the hidden columns, so pass B needs
+      // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
+      const bool masked_b = kCausal ? !(c > 0.f) : last;
+      if (kCausal) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
+      l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kBarPFull + t));
     }
 
     if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
-    const Work wk = work_of(p);
+    const Work wk = work_of<kCausal>(p);
     if (kPartial && ok) {
       // Split epilogue: this row's unnormalised fp32 output, the running max it is
       // relative to, and its row sum.

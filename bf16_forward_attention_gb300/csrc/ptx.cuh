@@ -310,6 +310,44 @@ __device__ __forceinline__ float min_nan(float a, float b) {
 
 // Packed pairs of fp32 (one 64-bit register pair; `lo` is the first element).
 // The f32x2 instructions round each lane to nearest like their scalar forms.
+// Masks a 16-column chunk of a TMEM row and writes it back: x[i] = fill for
+// every i >= rel (i = 0..15), then the 16 values are stored at taddr (32 lanes x
+// 16 columns), unless skip is set. skip must be the same on every lane of the
+// warp: the branch over the block is declared uniform, so the warp-collective
+// store is reached by all lanes or none. rel may differ per lane. The labels
+// are local to the asm block's scope.
+__device__ __forceinline__ void mask16_store_uniform(uint32_t (&x)[16], int rel, int skip,
+                                                     uint32_t fill, uint32_t taddr) {
+  asm volatile(
+      "{\n\t.reg .pred ps, pq;\n\t"
+      "setp.ne.s32 ps, %17, 0;\n\t"
+      "@ps bra.uni MASK16_DONE;\n\t"
+      "setp.le.s32 pq, %16, 0;\n\tselp.b32 %0, %18, %0, pq;\n\t"
+      "setp.le.s32 pq, %16, 1;\n\tselp.b32 %1, %18, %1, pq;\n\t"
+      "setp.le.s32 pq, %16, 2;\n\tselp.b32 %2, %18, %2, pq;\n\t"
+      "setp.le.s32 pq, %16, 3;\n\tselp.b32 %3, %18, %3, pq;\n\t"
+      "setp.le.s32 pq, %16, 4;\n\tselp.b32 %4, %18, %4, pq;\n\t"
+      "setp.le.s32 pq, %16, 5;\n\tselp.b32 %5, %18, %5, pq;\n\t"
+      "setp.le.s32 pq, %16, 6;\n\tselp.b32 %6, %18, %6, pq;\n\t"
+      "setp.le.s32 pq, %16, 7;\n\tselp.b32 %7, %18, %7, pq;\n\t"
+      "setp.le.s32 pq, %16, 8;\n\tselp.b32 %8, %18, %8, pq;\n\t"
+      "setp.le.s32 pq, %16, 9;\n\tselp.b32 %9, %18, %9, pq;\n\t"
+      "setp.le.s32 pq, %16, 10;\n\tselp.b32 %10, %18, %10, pq;\n\t"
+      "setp.le.s32 pq, %16, 11;\n\tselp.b32 %11, %18, %11, pq;\n\t"
+      "setp.le.s32 pq, %16, 12;\n\tselp.b32 %12, %18, %12, pq;\n\t"
+      "setp.le.s32 pq, %16, 13;\n\tselp.b32 %13, %18, %13, pq;\n\t"
+      "setp.le.s32 pq, %16, 14;\n\tselp.b32 %14, %18, %14, pq;\n\t"
+      "setp.le.s32 pq, %16, 15;\n\tselp.b32 %15, %18, %15, pq;\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%19], {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15};\n"
+      "MASK16_DONE:\n\t}"
+      : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]),
+        "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]),
+        "+r"(x[14]), "+r"(x[15])
+      : "r"(rel), "r"(skip), "r"(fill), "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));

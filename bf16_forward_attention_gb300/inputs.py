@@ -127,11 +127,31 @@ class Workload:
     roundings: tuple = ("rtne",)
     seed: int = 20260001
     splitkv: bool = False  # run with the key range split over CTAs
+    causal: bool = False   # key j visible to query i iff j <= i + Sk - Sq
+    hkv: int = 0           # key/value heads (grouped-query); 0 means H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.hkv or self.H
+
+    @property
+    def visible_pairs(self) -> int:
+        """(query, key) pairs one head computes: Sq*Sk, or under the causal mask
+        sum over rows i of clamp(i + Sk - Sq + 1, 0, Sk)."""
+        if not self.causal:
+            return self.Sq * self.Sk
+        # Rows i < lo see no key; row i >= lo sees i + off + 1 keys (at most Sk,
+        # reached by the last row).
+        off = self.Sk - self.Sq
+        lo = max(0, -off)
+        n = self.Sq - lo
+        return n * (lo + off + 1) + n * (n - 1) // 2
 
     @property
     def flops(self) -> int:
-        """Counted work of one call: 4*B*H*Sq*Sk*D (QK^T and PV, 2 flops per MAC)."""
-        return 4 * self.B * self.H * self.Sq * self.Sk * self.D
+        """Counted work of one call: 4*D per visible (query, key) pair and head
+        (QK^T and PV, 2 flops per MAC); 4*B*H*Sq*Sk*D without a mask."""
+        return 4 * self.B * self.H * self.visible_pairs * self.D
 
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -151,9 +171,15 @@ WORKLOADS = {
     "stress16381": Workload("stress16381", "bhsd", 4, 24, 16381, 16381, qk_std=8.0,
                             v_dist="uniform", specials=True, roundings=("rtz",),
                             seed=20260005),
-    # Follow-on workload for the split-KV path: few query rows against long keys.
+    # Follow-on workloads: few query rows against long keys (split-KV path), the
+    # 8K self-attention case under the causal mask, and with grouped-query heads
+    # (16 query heads sharing 4 key/value heads).
     "decode32k": Workload("decode32k", "bhsd", 1, 8, 256, 32768, roundings=("rtne",),
                           seed=20260006, splitkv=True),
+    "causal8k": Workload("causal8k", "bshd", 2, 16, 8192, 8192, roundings=("rtne",),
+                         seed=20260007, causal=True),
+    "gqa8k": Workload("gqa8k", "bshd", 2, 16, 8192, 8192, roundings=("rtne",),
+                      seed=20260008, hkv=4),
 }
 
 
@@ -164,7 +190,7 @@ def special_positions(w: Workload) -> list:
     for b in range(w.B):
         r = splitmix64(key, 8 * b, 6)
         qpos = (int(r[0] % np.uint64(w.H)), int(r[1] % np.uint64(w.Sq)), int(r[2] % np.uint64(w.D)))
-        kpos = (int(r[3] % np.uint64(w.H)), int(r[4] % np.uint64(w.Sk)), int(r[5] % np.uint64(w.D)))
+        kpos = (int(r[3] % np.uint64(w.kv_heads)), int(r[4] % np.uint64(w.Sk)), int(r[5] % np.uint64(w.D)))
         out.append((b, qpos, kpos))
     return out
 
@@ -172,7 +198,7 @@ def special_positions(w: Workload) -> list:
 def make_qkv(w: Workload) -> tuple:
     """Returns (q, k, v) as contiguous bf16 CPU tensors in the workload's layout."""
     nq = w.B * w.H * w.Sq * w.D
-    nk = w.B * w.H * w.Sk * w.D
+    nk = w.B * w.kv_heads * w.Sk * w.D
     q = normal_f32(w.seed, 0, nq, w.qk_std)
     k = normal_f32(w.seed, 1, nk, w.qk_std)
     if w.v_dist == "normal":
@@ -182,7 +208,7 @@ def make_qkv(w: Workload) -> tuple:
     else:
         raise ValueError(w.v_dist)
     qs = shape_of(w.layout, w.B, w.H, w.Sq, w.D)
-    ks = shape_of(w.layout, w.B, w.H, w.Sk, w.D)
+    ks = shape_of(w.layout, w.B, w.kv_heads, w.Sk, w.D)
     q = q.reshape(qs)
     k = k.reshape(ks)
     v = v.reshape(ks)

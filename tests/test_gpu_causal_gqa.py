@@ -76,3 +76,12 @@ def test_causal_wide_logits_and_negative_scale():
         torch.cuda.synchronize()
         exact = attention_fp64(f64_of(q), f64_of(k), f64_of(v), scale, "bhsd", causal=True)
         assert_parity(compare(bits_of(out), exact, "rtz"), max_abs_err=None)
+
+
+def test_causal_zero_scale_is_mean_of_visible_rows():
+    # scale 0: every visible logit is 0, so each row is the mean of its visible V rows.
+    q, k, v = _qkv("bshd", 1, 2, 2, 300, 420, seed=953)
+    out = attn.attn_fwd_ex(q.cuda(), k.cuda(), v.cuda(), causal=True, layout="bshd", scale=0.0)
+    torch.cuda.synchronize()
+    exact = attention_fp64(f64_of(q), f64_of(k), f64_of(v), 0.0, "bshd", causal=True)
+    assert_parity(compare(bits_of(out), exact, "rtne"), excess=True)
