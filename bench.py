@@ -1,7 +1,7 @@
 """Benchmark: bf16 forward attention on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload self8k|cross4k32k|long128k|stress16381|tiny|decode32k|causal8k|gqa8k]
+                    [--workload self8k|cross4k32k|long128k|stress16381|tiny|decode32k|causal8k|gqa8k|varlen16]
 
 Workload (default): self-attention, BSHD, B=2, H=16, Sq=Sk=8192, d=128, bf16
 Q/K/V ~ N(0,1) from a fixed seed, scale 1/sqrt(128). One step = one call of the
@@ -146,8 +146,10 @@ def _cpu_sample(w, q, k, v, budget_s: float):
     from oracle import attention_rows_fp64, bf16_bits_to_f64, to_bhsd
     from bf16_forward_attention_gb300 import inputs
 
-    qb, kb, vb = (to_bhsd(t.view(torch.int16).numpy(), w.layout) for t in (q, k, v))
     scale = inputs.default_scale()
+    if w.seqlens:
+        return _cpu_sample_varlen(w, q, k, v, budget_s, scale)
+    qb, kb, vb = (to_bhsd(t.view(torch.int16).numpy(), w.layout) for t in (q, k, v))
     rows_done, pairs, t_used, i = 0, 0, 0.0, 0
     block = 256
     group = w.H // w.kv_heads
@@ -168,12 +170,52 @@ def _cpu_sample(w, q, k, v, budget_s: float):
     return 4.0 * pairs * w.D, t_used, rows_done
 
 
+def _cpu_sample_varlen(w, q, k, v, budget_s, scale):
+    """The oracle on a packed variable-length batch: blocks of rows of successive
+    (sequence, head) pairs, each against its sequence's keys."""
+    from oracle import attention_rows_fp64, bf16_bits_to_f64
+
+    cq, ck = w.cu_seqlens
+    qn, kn, vn = (t.view(torch.int16).numpy() for t in (q, k, v))
+    group = w.H // w.kv_heads
+    items = [(b, h) for b in range(w.B) for h in range(w.H) if cq[b + 1] > cq[b] and ck[b + 1] > ck[b]]
+    rows_done, pairs, t_used, i = 0, 0, 0.0, 0
+    while t_used < budget_s:
+        b, h = items[i % len(items)]
+        sq, sk = int(cq[b + 1] - cq[b]), int(ck[b + 1] - ck[b])
+        r0 = ((i // len(items)) * 256) % sq
+        rows = np.arange(r0, min(sq, r0 + 256))
+        qh = bf16_bits_to_f64(qn[cq[b]:cq[b + 1], h])
+        kh = bf16_bits_to_f64(kn[ck[b]:ck[b + 1], h // group])
+        vh = bf16_bits_to_f64(vn[ck[b]:ck[b + 1], h // group])
+        t0 = time.perf_counter()
+        attention_rows_fp64(qh, kh, vh, scale, rows, causal=w.causal)
+        t_used += time.perf_counter() - t0
+        rows_done += rows.size
+        pairs += (int(np.clip(rows + (sk - sq) + 1, 0, sk).sum()) if w.causal else rows.size * sk)
+        i += 1
+    return 4.0 * pairs * w.D, t_used, rows_done
+
+
 def _keys_seen(w):
     return f"its visible keys of {w.Sk} (causal)" if w.causal else f"all {w.Sk} keys"
 
 
 def _config(w, world):
     big = 3 * 2 * w.B * w.H * max(w.Sq, w.Sk) * w.D > L2_BYTES
+    if w.seqlens:
+        lens = [a for a, _ in w.seqlens]
+        return {"workload": f"{w.name}: variable-length self-attention fwd, packed tokens "
+                            f"(token, head, d), {w.B} sequences of {min(lens)}..{max(lens)} tokens "
+                            f"({sum(lens)} in all), H={w.H}, d={w.D}"
+                            + (", causal mask" if w.causal else "")
+                            + f", rounding {'/'.join(m.upper() for m in w.roundings)}",
+                "layout": "packed", "B": w.B, "H": w.H, "H_kv": w.kv_heads, "d": w.D,
+                "seqlens": lens, "causal": w.causal, "roundings": list(w.roundings),
+                "calls_per_step": len(w.roundings), "qk_dist": f"N(0,{w.qk_std:g}^2)",
+                "v_dist": "N(0,1)", "seed": w.seed,
+                "l2": "inputs larger than L2 (not flushed)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     return {"workload": f"{w.name}: {'self' if w.Sq == w.Sk else 'cross'}-attention fwd, "
                         f"{w.layout.upper()}, B={w.B}, H={w.H}, Sq={w.Sq}, Sk={w.Sk}, d={w.D}, "
                         + (f"{w.kv_heads} key/value heads, " if w.kv_heads != w.H else "")
@@ -242,7 +284,16 @@ def run_ours(args, w):
         workspace = torch.empty(max(16, attn.splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, splits)),
                                 dtype=torch.uint8, device=dev)
 
-    def call(qq, kk, vv, m, out=None):
+    cu_dev = None
+    if w.seqlens:
+        cu_dev = tuple(torch.from_numpy(a).to(dev) for a in w.cu_seqlens)
+        max_sq = max(a for a, _ in w.seqlens)
+
+    def call(qq, kk, vv, m, out=None, cu=None):
+        if w.seqlens:
+            cqd, ckd = cu if cu is not None else cu_dev
+            return attn.attn_fwd_varlen(qq, kk, vv, cqd, ckd, max_sq, causal=w.causal, rounding=m,
+                                        out=out)
         if splits > 1:
             return attn.attn_fwd_splitkv(qq, kk, vv, num_splits=splits, layout=w.layout,
                                          rounding=m, out=out, workspace=workspace)
@@ -303,10 +354,13 @@ def run_ours(args, w):
     qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
     host_out = {m: torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory() for m in w.roundings}
 
+    cu_pinned = tuple(torch.from_numpy(a).pin_memory() for a in w.cu_seqlens) if w.seqlens else ()
+
     def e2e_step():
         qd, kd, vd = (t.to(dev, non_blocking=True) for t in (qp, kp, vp))
+        cu = tuple(t.to(dev, non_blocking=True) for t in cu_pinned) or None
         for m in w.roundings:
-            host_out[m].copy_(call(qd, kd, vd, m), non_blocking=True)
+            host_out[m].copy_(call(qd, kd, vd, m, cu=cu), non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -320,7 +374,8 @@ def run_ours(args, w):
     e_ms = e0.elapsed_time(e1) / e_steps
     e2e = {"value": flops_call * len(w.roundings) / (e_ms * 1e-3) / 1e12, "unit": UNIT,
            "ms_per_step": e_ms,
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h)),
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size()
+                                     for t in (q_h, k_h, v_h) + cu_pinned),
            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values())}
 
     peaks, peak_src = _peaks()

@@ -28,6 +28,7 @@ ATTN_ERR_LAUNCH = -7
 ATTN_ERR_TIMEOUT = -8
 ATTN_ERR_TOO_LARGE = -9
 ATTN_ERR_SCRATCH = -10
+ATTN_ERR_SEQLENS = -11
 ATTN_FLAG_CAUSAL = 1
 
 _lib = None
@@ -81,6 +82,9 @@ def load_library() -> ctypes.CDLL:
                                                         ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                         ctypes.c_void_p]
     lib.attn_fwd_ex.restype = ctypes.c_int
+    lib.attn_fwd_varlen.argtypes = ([ctypes.c_void_p] * 6 + [i64] * 7
+                                    + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p])
+    lib.attn_fwd_varlen.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -221,6 +225,61 @@ def attn_fwd_ex(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     return out
 
 
+def attn_fwd_varlen_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, cu_q_ptr: int,
+                        cu_k_ptr: int, B: int, Hq: int, Hkv: int, total_q: int, total_k: int,
+                        max_seqlen_q: int, d: int, scale: float, rounding_mode: int, flags: int,
+                        stream: int) -> int:
+    """Direct call of ``attn_fwd_varlen`` (packed variable-length batch)."""
+    return load_library().attn_fwd_varlen(q_ptr, k_ptr, v_ptr, out_ptr, cu_q_ptr, cu_k_ptr, B, Hq,
+                                          Hkv, total_q, total_k, max_seqlen_q, d,
+                                          ctypes.c_float(scale), rounding_mode, flags, stream)
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, *,
+                    causal: bool = False, scale: float | None = None, rounding: str = "rtne",
+                    out=None):
+    """Attention over a packed batch of variable-length sequences.
+
+    q: (total_q, Hq, 128), k and v: (total_k, Hkv, 128), bf16 CUDA tensors packed
+    token after token; cu_seqlens_q / cu_seqlens_k: int32 CUDA tensors of B + 1
+    offsets; max_seqlen_q: a bound on every sequence's query count. Invalid
+    offsets are found on the device: check ``attn_fwd_last_error()`` after a sync.
+    """
+    import torch
+
+    if rounding not in ROUNDINGS:
+        raise ValueError("unknown rounding mode")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous (tokens, heads, d) tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda
+                or t.dim() != 1 or not t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous 1-D int32 CUDA tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 >= 2 entries")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    if Dk != D or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_varlen_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                                 cu_seqlens_q.numel() - 1, Hq, Hkv, total_q, total_k,
+                                 int(max_seqlen_q), D, float(scale), ROUNDINGS[rounding],
+                                 ATTN_FLAG_CAUSAL if causal else 0, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, status_str(st))
+    return out
+
+
 def attn_fwd_last_error() -> int:
     return load_library().attn_fwd_last_error()
 
@@ -277,5 +336,6 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
 
 __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw",
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
-           "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "status_str", "load_library",
+           "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw",
+           "attn_fwd_varlen", "attn_fwd_varlen_raw", "ATTN_ERR_SEQLENS", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

@@ -56,10 +56,14 @@ int device_ready(int dev) {
     g_dev_state[dev] = ATTN_ERR_ARCH;
     return ATTN_ERR_ARCH;
   }
-  // Every variant of the fused kernel (whole key range / split; causal).
-  const void* variants[] = {reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false>),
-                            reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false>),
-                            reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true>)};
+  // Every variant of the fused kernel (whole key range / split; causal; packed
+  // variable-length batch, without and with the causal mask).
+  const void* variants[] = {
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>)};
   for (const void* fn : variants) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) !=
         cudaSuccess) {
@@ -143,6 +147,7 @@ const char* attn_status_str(int status) {
     case ATTN_ERR_TIMEOUT: return "a device-side wait timed out";
     case ATTN_ERR_TOO_LARGE: return "size beyond tensor-map or grid limits";
     case ATTN_ERR_SCRATCH: return "split workspace needed exceeds the library's fixed 32 MiB device scratch";
+    case ATTN_ERR_SEQLENS: return "invalid cu_seqlens contents (found on the device; those sequences were not computed)";
     default: return "unknown status";
   }
 }
@@ -226,15 +231,22 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.group = static_cast<int>(H / Hkv);
   p.causal = causal ? 1 : 0;
   p.causal_off = static_cast<int>(Sk - Sq);
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.max_sq = p.Sq;
+  p.out = static_cast<uint16_t*>(out);
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
   if (causal) {
-    attn::attn_fwd_kernel<false, true><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+    attn::attn_fwd_kernel<false, true, false>
+        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
   } else if (n_splits == 1) {
-    attn::attn_fwd_kernel<false, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+    attn::attn_fwd_kernel<false, false, false>
+        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
   } else {
-    attn::attn_fwd_kernel<true, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+    attn::attn_fwd_kernel<true, false, false>
+        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
     attn::CombineParams cp;
     cp.part_o = p.part_o;
     cp.part_rl = p.part_rl;
@@ -271,6 +283,93 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layo
   if (Hkv < 1) return ATTN_ERR_INVALID_ARG;
   return attn_fwd_impl(q, k, v, out, layout, B, Hq, Sq, Sk, d, scale, rounding_mode, stream,
                        kTimeoutNs, 0, 1, nullptr, 0, Hkv, (flags & ATTN_FLAG_CAUSAL) ? 1 : 0);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t B,
+                    int64_t Hq, int64_t Hkv, int64_t total_q, int64_t total_k,
+                    int64_t max_seqlen_q, int64_t d, float scale, int rounding_mode, int flags,
+                    void* stream) {
+  // ---- host-side validation (nothing is launched on failure); the offsets
+  // themselves live on the device and are checked by the kernel.
+  if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (total_q < 1 || total_k < 1 || max_seqlen_q < 1 || max_seqlen_q > total_q)
+    return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_CAUSAL) return ATTN_ERR_UNSUPPORTED;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (rounding_mode < ATTN_ROUND_RTNE || rounding_mode > ATTN_ROUND_RTZ) return ATTN_ERR_UNSUPPORTED;
+  const int64_t kLim31 = (int64_t(1) << 31) - 1;
+  if (total_q > kLim31 || total_k > kLim31 || Hq > kLim31 || B > kLim31) return ATTN_ERR_TOO_LARGE;
+  const int64_t kStrideLim = int64_t(1) << 40;
+  if (Hq > kStrideLim / 256 / total_q || Hkv > kStrideLim / 256 / total_k) return ATTN_ERR_TOO_LARGE;
+  const int64_t n_qpairs = qpairs_of(max_seqlen_q);
+  if (B * Hq > kLim31 / n_qpairs) return ATTN_ERR_TOO_LARGE;
+  const uintptr_t ormask = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (ormask & 15u) return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k)) & 3u)
+    return ATTN_ERR_MISALIGNED;
+  const uint64_t bytes_q = uint64_t(total_q) * Hq * 256, bytes_kv = uint64_t(total_k) * Hkv * 256;
+  if (overlaps(out, bytes_q, q, bytes_q) || overlaps(out, bytes_q, k, bytes_kv) ||
+      overlaps(out, bytes_q, v, bytes_kv) ||
+      overlaps(out, bytes_q, cu_seqlens_q, uint64_t(B + 1) * 4) ||
+      overlaps(out, bytes_q, cu_seqlens_k, uint64_t(B + 1) * 4))
+    return ATTN_ERR_ALIASING;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  const int st = device_ready(dev);
+  if (st != ATTN_OK) return st;
+
+  // The packed tensors are BSHD with one batch entry and S = total tokens.
+  CUtensorMap tq, tk, tv, to;
+  const int lay = ATTN_LAYOUT_BSHD;
+  if (!make_map(&tq, q, lay, 1, Hq, total_q, attn::kBM) ||
+      !make_map(&tk, k, lay, 1, Hkv, total_k, attn::kBN) ||
+      !make_map(&tv, v, lay, 1, Hkv, total_k, attn::kBN) ||
+      !make_map(&to, out, lay, 1, Hq, total_q, 32))
+    return ATTN_ERR_LAUNCH;
+
+  attn::Params p;
+  p.Sq = static_cast<int>(total_q);
+  p.Sk = static_cast<int>(total_k);
+  p.H = static_cast<int>(Hq);
+  p.n_qpairs = static_cast<int>(n_qpairs);
+  p.kv_tiles = static_cast<int>(kv_tiles_of(total_k));
+  p.kv_tail = static_cast<int>(total_k - int64_t(p.kv_tiles - 1) * attn::kBN);
+  p.n_splits = 1;
+  p.BH = static_cast<int>(B * Hq);
+  p.sq_pad = 0;
+  p.part_o = nullptr;
+  p.part_rl = nullptr;
+  p.layout = lay;
+  p.mode = rounding_mode;
+  p.c = scale * 1.4426950408889634f;
+  p.timeout_ns = kTimeoutNs;
+  p.withhold_s0 = 0;
+  p.group = static_cast<int>(Hq / Hkv);
+  p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
+  p.causal_off = 0;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.max_sq = static_cast<int>(max_seqlen_q);
+  p.out = static_cast<uint16_t*>(out);
+
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(B * Hq * n_qpairs);
+  if (p.causal)
+    attn::attn_fwd_kernel<false, true, true>
+        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+  else
+    attn::attn_fwd_kernel<false, false, true>
+        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
+  return ATTN_OK;
 }
 
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
@@ -327,7 +426,7 @@ int attn_fwd_last_error(void) {
   if (s == 0) return ATTN_OK;
   const unsigned int zero = 0;
   cudaMemcpyToSymbol(attn::g_attn_status, &zero, sizeof(zero));
-  return ATTN_ERR_TIMEOUT;
+  return (s & 1u) ? ATTN_ERR_TIMEOUT : ATTN_ERR_SEQLENS;
 }
 
 }  // extern "C"

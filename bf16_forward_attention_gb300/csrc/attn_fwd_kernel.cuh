@@ -105,9 +105,16 @@ struct Params {
   int group;        // query heads per key/value head (grouped-query attention)
   int causal;       // 1: key j visible to query i iff j <= i + causal_off
   int causal_off;   // Sk - Sq
+  // Variable-length batch (packed tokens; the tensor maps then have B = 1 and
+  // S = total tokens, and B above is the number of sequences):
+  const int* cu_q;  // B + 1 query offsets (device memory)
+  const int* cu_k;  // B + 1 key offsets
+  int max_sq;       // bound on every sequence's query length (sizes the grid)
+  uint16_t* out;    // output base, for rows stored without TMA
 };
 
-// Bit 0: some wait timed out.
+// Bit 0: some wait timed out. Bit 1: a variable-length batch's offsets were
+// invalid (that sequence's output is left unwritten).
 __device__ unsigned int g_attn_status;
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start,
@@ -388,14 +395,17 @@ struct Work {
   int split, pair, bh, head, kv_head, batch;
   int tile0, n_kv;  // key tiles [tile0, tile0 + n_kv)
   bool has_tail;    // this split holds the ragged last key tile
+  int q_base, k_base;  // first query / key token of the sequence (varlen; else 0)
+  int sq, sk;          // the sequence's query / key lengths
+  bool bad;            // varlen: the offsets of this sequence are invalid
 };
 
-template <bool kCausal>
+template <bool kCausal, bool kVarlen>
 __device__ __forceinline__ Work work_of(const Params& p) {
   Work w;
   w.split = blockIdx.x % p.n_splits;
   const int item = blockIdx.x / p.n_splits;
-  if (kCausal) {
+  if (kCausal || kVarlen) {
     // Longest key ranges first over the whole grid (blocks start in index order).
     w.pair = p.n_qpairs - 1 - item / p.BH;
     w.bh = item % p.BH;
@@ -406,16 +416,36 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   w.head = w.bh % p.H;
   w.kv_head = w.head / p.group;
   w.batch = w.bh / p.H;
-  const int base = p.kv_tiles / p.n_splits, rem = p.kv_tiles % p.n_splits;
+  int kv_tiles = p.kv_tiles;
+  if (kVarlen) {
+    // The sequence's tokens within the packed tensors. At least one key tile
+    // runs (fully masked if the sequence has no key, so its rows come out NaN).
+    const int b = w.batch;
+    w.q_base = __ldg(p.cu_q + b);
+    w.sq = __ldg(p.cu_q + b + 1) - w.q_base;
+    w.k_base = __ldg(p.cu_k + b);
+    w.sk = __ldg(p.cu_k + b + 1) - w.k_base;
+    w.bad = w.q_base < 0 || w.sq < 0 || w.sq > p.max_sq || w.q_base + w.sq > p.Sq ||
+            w.k_base < 0 || w.sk < 0 || w.k_base + w.sk > p.Sk;
+    w.batch = 0;
+    kv_tiles = w.sk > 0 ? (w.sk + kBN - 1) / kBN : 1;
+  } else {
+    w.q_base = 0;
+    w.k_base = 0;
+    w.sq = p.Sq;
+    w.sk = p.Sk;
+    w.bad = false;
+  }
+  const int base = kv_tiles / p.n_splits, rem = kv_tiles % p.n_splits;
   w.tile0 = w.split * base + (w.split < rem ? w.split : rem);
   w.n_kv = base + (w.split < rem ? 1 : 0);
   if (kCausal) {
     // Key tiles up to the diagonal of the pair's last row (at least one, so that
     // a row with no visible key still runs and comes out NaN).
-    const int last_row = min(p.Sq, 2 * kBM * (w.pair + 1)) - 1;
-    const int visible = last_row + p.causal_off + 1;
+    const int last_row = min(w.sq, 2 * kBM * (w.pair + 1)) - 1;
+    const int visible = last_row + (w.sk - w.sq) + 1;
     const int tiles = visible <= 0 ? 1 : (visible + kBN - 1) / kBN;
-    w.n_kv = min(tiles, p.kv_tiles);
+    w.n_kv = min(tiles, kv_tiles);
   }
   w.has_tail = w.tile0 + w.n_kv == p.kv_tiles && p.kv_tail < kBN;
   return w;
@@ -424,8 +454,10 @@ __device__ __forceinline__ Work work_of(const Params& p) {
 // kPartial: the CTA covers one split of the key range and writes its fp32 partial
 // result to the workspace (combined by attn_splitkv_combine); otherwise the CTA
 // covers all keys and stores bf16 output. kCausal: the causal mask (p.causal
-// must agree); compiled separately so that the other variants carry none of it.
-template <bool kPartial, bool kCausal>
+// must agree). kVarlen: a packed batch of variable-length sequences, one grid
+// slot per (sequence, head, query-tile pair) up to the longest sequence. Each is
+// compiled separately so that the other variants carry none of it.
+template <bool kPartial, bool kCausal, bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -442,7 +474,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A key limit per row (rising along the causal diagonal, or the sequence's
+  // key count) selects pass-A masking in every tile.
+  constexpr bool kRowLimit = kCausal || kVarlen;
 
+  if constexpr (kVarlen) {
+    // Grid slots past the sequence's queries, and sequences with invalid
+    // offsets, leave before anything is set up (the decision is the same for
+    // every thread of the CTA).
+    const Work wk = work_of<kCausal, kVarlen>(p);
+    if (wk.bad) {
+      if (threadIdx.x == 0) atomicOr(&g_attn_status, 2u);
+      return;
+    }
+    if (2 * kBM * wk.pair >= wk.sq) return;
+  }
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(kBarQ), 1);
@@ -482,14 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        const Work wk = work_of<kCausal>(p);
+        const Work wk = work_of<kCausal, kVarlen>(p);
         const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
-        const int kv_head = wk.kv_head;
+        const int kv_head = wk.kv_head, q_base = wk.q_base, k_base = wk.k_base;
         int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
         int c1, c2;
         ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
         for (int t = 0; t < kQTiles; ++t) {
-          tma_coords(p.layout, (2 * pair + t) * kBM, head, c1, c2);
+          tma_coords(p.layout, q_base + (2 * pair + t) * kBM, head, c1, c2);
           for (int hf = 0; hf < 2; ++hf)
             ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
                              batch);
@@ -499,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t parity = ((it / kStages) & 1) ^ 1;
           if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
           const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-          tma_coords(p.layout, (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
+          tma_coords(p.layout, k_base + (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
           ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
             ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
@@ -519,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        const int n_kv = work_of<kCausal>(p).n_kv;
+        const int n_kv = work_of<kCausal, kVarlen>(p).n_kv;
         bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
         ptx::tc_fence_after();
         auto ring_wait = [&](int it) -> bool {
@@ -597,11 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int n_kv, row_lim;
     {
-      const Work wk = work_of<kCausal>(p);
+      const Work wk = work_of<kCausal, kVarlen>(p);
       n_kv = wk.n_kv;  // key tiles of this CTA
-      // Causal: number of keys this row sees, counted from key 0 (capped at Sk,
-      // which also hides the ragged tail from the padding rows past Sq).
-      row_lim = kCausal ? min((2 * wk.pair + t) * kBM + row + p.causal_off + 1, p.Sk) : 0;
+      // Number of keys this row sees, counted from the sequence's key 0: the
+      // causal limit (capped at Sk, which also hides the ragged tail from the
+      // padding rows past Sq), or for a variable-length batch without the mask
+      // the sequence's key count (hiding the next sequence's keys).
+      row_lim = kCausal ? min((2 * wk.pair + t) * kBM + row + (wk.sk - wk.sq) + 1, wk.sk)
+                        : (kVarlen ? wk.sk : 0);
     }
 
     for (int j = 0; j < n_kv; ++j) {
@@ -615,11 +664,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Masked tile: the ragged last tile; with the causal mask every tile, each
       // row hiding the keys beyond its own limit (a tile it fully sees loses
       // nothing). One path for all tiles keeps the loop's registers spill-free.
-      const bool masked = kCausal ? true : last;
-      constexpr int kM = kCausal ? kChunkMask : kElemMask;
-      const int valid = kCausal ? row_lim - kBN * j : p.kv_tail;
+      const bool masked = kRowLimit ? true : last;
+      constexpr int kM = kRowLimit ? kChunkMask : kElemMask;
+      const int valid = kRowLimit ? row_lim - kBN * j : p.kv_tail;
       // Least `valid` over the warp (lane 0 has the warp's first row).
-      const int vmin = kCausal ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
+      const int vmin = kRowLimit ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
       // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
       // holds exactly that tile: the MMA that wrote S_j was issued after
       // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
@@ -647,8 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
       // Causal, c > 0: pass A left -Inf in the hidden columns, so pass B needs
       // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
-      const bool masked_b = kCausal ? !(c > 0.f) : last;
-      if (kCausal) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
+      const bool masked_b = kRowLimit ? !(c > 0.f) : last;
+      if (kRowLimit) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
       l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -656,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
-    const Work wk = work_of<kCausal>(p);
+    const Work wk = work_of<kCausal, kVarlen>(p);
     if (kPartial && ok) {
       // Split epilogue: this row's unnormalised fp32 output, the running max it is
       // relative to, and its row sum.
@@ -705,16 +754,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;
-        if (q_row0 < p.Sq) {
+      const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;  // within the sequence
+      if (!kVarlen || q_row0 + 32 <= wk.sq) {
+        if (lane == 0 && q_row0 < wk.sq) {
           int c1, c2;
-          tma_coords(p.layout, q_row0, wk.head, c1, c2);
+          tma_coords(p.layout, wk.q_base + q_row0, wk.head, c1, c2);
           for (int hf = 0; hf < 2; ++hf)
             ptx::tma_store_4d(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1, c2,
                               wk.batch);
           ptx::bulk_commit_group();
           ptx::bulk_wait_group_0();
+        }
+      } else if (lane < wk.sq - q_row0) {
+        // The sequence ends inside this warp's rows: a TMA box would run into the
+        // next sequence's rows, so each row up to the end is copied out of the
+        // staging buffer with plain 16-byte stores (packed layout: token, head).
+        const uint8_t* stage = smem + (stage_base - sbase);
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + (static_cast<size_t>(wk.q_base + q_row0 + lane) * p.H + wk.head) * kD);
+#pragma unroll
+        for (int cix = 0; cix < 16; ++cix) {
+          const int off = (cix >> 3) * kHalfBytes + row * 128 + (((cix & 7) ^ (row & 7)) << 4);
+          dst[cix] = *reinterpret_cast<const uint4*>(stage + off);
         }
       }
       __syncwarp();

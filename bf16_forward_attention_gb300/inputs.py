@@ -29,6 +29,8 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
 LAYOUTS = ("bhsd", "bshd")
+# Variable-length batches are packed token after token: (total tokens, heads, d),
+# sequence b owning tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.
 ROUNDINGS = ("rtne", "rtna", "rtz")
 
 
@@ -129,6 +131,8 @@ class Workload:
     splitkv: bool = False  # run with the key range split over CTAs
     causal: bool = False   # key j visible to query i iff j <= i + Sk - Sq
     hkv: int = 0           # key/value heads (grouped-query); 0 means H
+    seqlens: tuple = ()    # variable-length batch: per-sequence (Sq_b, Sk_b); B, Sq, Sk
+                           # then hold the count and the longest lengths
 
     @property
     def kv_heads(self) -> int:
@@ -137,7 +141,11 @@ class Workload:
     @property
     def visible_pairs(self) -> int:
         """(query, key) pairs one head computes: Sq*Sk, or under the causal mask
-        sum over rows i of clamp(i + Sk - Sq + 1, 0, Sk)."""
+        sum over rows i of clamp(i + Sk - Sq + 1, 0, Sk). For a variable-length
+        batch the sum over its sequences (then per head, not per batch entry)."""
+        if self.seqlens:
+            return sum(dataclasses.replace(self, seqlens=(), B=1, Sq=a, Sk=b).visible_pairs
+                       for a, b in self.seqlens)
         if not self.causal:
             return self.Sq * self.Sk
         # Rows i < lo see no key; row i >= lo sees i + off + 1 keys (at most Sk,
@@ -151,10 +159,25 @@ class Workload:
     def flops(self) -> int:
         """Counted work of one call: 4*D per visible (query, key) pair and head
         (QK^T and PV, 2 flops per MAC); 4*B*H*Sq*Sk*D without a mask."""
+        if self.seqlens:
+            return 4 * self.H * self.visible_pairs * self.D
         return 4 * self.B * self.H * self.visible_pairs * self.D
+
+    @property
+    def cu_seqlens(self) -> tuple:
+        """(cu_seqlens_q, cu_seqlens_k) of a variable-length batch, as int32 arrays."""
+        cq = np.concatenate([[0], np.cumsum([a for a, _ in self.seqlens])]).astype(np.int32)
+        ck = np.concatenate([[0], np.cumsum([b for _, b in self.seqlens])]).astype(np.int32)
+        return cq, ck
 
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
+
+
+def varlen_lengths(seed: int, n: int, lo: int, hi: int) -> tuple:
+    """n seeded sequence lengths, uniform on the integers lo..hi."""
+    r = splitmix64(stream_key(seed, 7), 0, n)
+    return tuple(int(lo + int(x % np.uint64(hi - lo + 1))) for x in r)
 
 
 # The five synthetic workloads: a tiny self-attention case, the 8K self-attention
@@ -181,6 +204,12 @@ WORKLOADS = {
     "gqa8k": Workload("gqa8k", "bshd", 2, 16, 8192, 8192, roundings=("rtne",),
                       seed=20260008, hkv=4),
 }
+# Variable-length self-attention batch: 16 sequences of seeded lengths 256..16384
+# (a mix around the 8K case), 16 heads, packed token after token.
+_VL = varlen_lengths(20260009, 16, 256, 16384)
+WORKLOADS["varlen16"] = Workload("varlen16", "thd", len(_VL), 16, max(_VL), max(_VL),
+                                 roundings=("rtne",), seed=20260009,
+                                 seqlens=tuple((n, n) for n in _VL))
 
 
 def special_positions(w: Workload) -> list:
@@ -196,7 +225,15 @@ def special_positions(w: Workload) -> list:
 
 
 def make_qkv(w: Workload) -> tuple:
-    """Returns (q, k, v) as contiguous bf16 CPU tensors in the workload's layout."""
+    """Returns (q, k, v) as contiguous bf16 CPU tensors in the workload's layout
+    (a variable-length batch: packed (total, heads, D))."""
+    if w.seqlens:
+        tq = sum(a for a, _ in w.seqlens)
+        tk = sum(b for _, b in w.seqlens)
+        q = normal_f32(w.seed, 0, tq * w.H * w.D, w.qk_std).reshape(tq, w.H, w.D)
+        k = normal_f32(w.seed, 1, tk * w.kv_heads * w.D, w.qk_std).reshape(tk, w.kv_heads, w.D)
+        v = normal_f32(w.seed, 2, tk * w.kv_heads * w.D, 1.0).reshape(tk, w.kv_heads, w.D)
+        return to_bf16(q), to_bf16(k), to_bf16(v)
     nq = w.B * w.H * w.Sq * w.D
     nk = w.B * w.kv_heads * w.Sk * w.D
     q = normal_f32(w.seed, 0, nq, w.qk_std)

@@ -39,8 +39,8 @@ typedef enum { ATTN_LAYOUT_BHSD = 0, ATTN_LAYOUT_BSHD = 1 } attn_layout_t;
  *   bf16 subnormals are kept. */
 typedef enum { ATTN_ROUND_RTNE = 0, ATTN_ROUND_RTNA = 1, ATTN_ROUND_RTZ = 2 } attn_round_t;
 
-/* Status codes. Errors other than ATTN_ERR_LAUNCH and ATTN_ERR_TIMEOUT are
- * found on the host before anything is launched. */
+/* Status codes. Errors other than ATTN_ERR_LAUNCH, ATTN_ERR_TIMEOUT and
+ * ATTN_ERR_SEQLENS are found on the host before anything is launched. */
 enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = -1, /* null pointer, a size < 1, non-finite scale     */
@@ -52,7 +52,9 @@ enum {
   ATTN_ERR_LAUNCH = -7,      /* the CUDA launch (or tensor-map setup) failed   */
   ATTN_ERR_TIMEOUT = -8,     /* a bounded device-side wait expired             */
   ATTN_ERR_TOO_LARGE = -9,   /* a size beyond the tensor-map / grid limits     */
-  ATTN_ERR_SCRATCH = -10     /* attn_fwd_splitkv_noalloc: workspace > 32 MiB   */
+  ATTN_ERR_SCRATCH = -10,    /* attn_fwd_splitkv_noalloc: workspace > 32 MiB   */
+  ATTN_ERR_SEQLENS = -11     /* attn_fwd_varlen: invalid offsets, found on the
+                                device and reported by attn_fwd_last_error     */
 };
 
 /*
@@ -129,6 +131,41 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, int
                      int rounding_mode, int num_splits, void* workspace, int64_t workspace_bytes,
                      void* stream);
 
+/*
+ * attn_fwd_varlen - attention over a packed batch of variable-length sequences,
+ * the follow-on step the pages call varlen batching and list as missing
+ * (snilld.dk, "Hvad er udgivet" and "Autoregressiv serving, de praktiske
+ * hager": serving mixes sequence lengths in one batch).
+ *
+ *   q    device, bf16, total_q * Hq * d elements, token-major: (token, head, d)
+ *   k, v device, bf16, total_k * Hkv * d elements, token-major
+ *   out  device, bf16, like q (written; must not overlap q, k, v or the offsets)
+ *   cu_seqlens_q, cu_seqlens_k
+ *        device, int32, B + 1 entries each: sequence b owns query tokens
+ *        cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens cu_seqlens_k[b] ..
+ *        cu_seqlens_k[b+1]-1, and attends only within itself. Offsets start at
+ *        0, do not decrease and end at total_q / total_k; a sequence may have no
+ *        queries (nothing to do) or no keys (its rows come out NaN).
+ *   B             number of sequences, >= 1
+ *   Hq, Hkv       query and key/value heads, as attn_fwd_ex
+ *   total_q, total_k   packed token counts, each >= 1
+ *   max_seqlen_q  an upper bound on every sequence's query count (1 .. total_q);
+ *                 it sizes the grid (a loose bound only adds grid slots that
+ *                 exit at once)
+ *   flags         0 or ATTN_FLAG_CAUSAL; the causal alignment is per sequence
+ *                 (key j visible to query i iff j <= i + Sk_b - Sq_b)
+ * The offsets stay on the device: the kernel checks each sequence's offsets
+ * against the totals and max_seqlen_q, skips a sequence whose offsets are
+ * invalid (its rows of out are left unwritten) and raises a device status that
+ * attn_fwd_last_error() returns as ATTN_ERR_SEQLENS. Other arguments,
+ * ownership, errors and the numerics contract as attn_fwd.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t B,
+                    int64_t Hq, int64_t Hkv, int64_t total_q, int64_t total_k,
+                    int64_t max_seqlen_q, int64_t d, float scale, int rounding_mode, int flags,
+                    void* stream);
+
 /* Workspace bytes attn_fwd_splitkv needs (0 for num_splits == 1), or a negative
  * status code for invalid sizes. Host only. */
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
@@ -170,10 +207,11 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
 const char* attn_status_str(int status);
 
 /*
- * Device-side status of earlier launches on the current device: ATTN_OK, or
+ * Device-side status of earlier launches on the current device: ATTN_OK;
  * ATTN_ERR_TIMEOUT if some launch gave up on a wait that did not finish within
  * its time limit (the kernel then stops its work, waits for its own copies in
- * flight, frees its tensor memory and returns; its output is undefined).
+ * flight, frees its tensor memory and returns; its output is undefined); else
+ * ATTN_ERR_SEQLENS if an attn_fwd_varlen launch found invalid offsets.
  * Reading clears the status. Synchronize the stream that ran the calls first.
  */
 int attn_fwd_last_error(void);

@@ -17,6 +17,7 @@ from .attention import (  # noqa: F401
     MODES,
     attention_fp64,
     attention_rows_fp64,
+    attention_varlen_fp64,
     bf16_bits_to_f64,
     nonfinite_bits,
     round_bf16,

@@ -32,6 +32,12 @@ Readings where the pages are silent (each is listed in the design notes):
     query see every key; hidden logits are -Inf, so a row that sees no key is NaN.
   * grouped-query attention (also named as missing): Hq query heads share Hkv
     key/value heads, query head h reads K/V head h // (Hq // Hkv).
+  * variable-length batches (also named as missing, as cu_seqlens batching):
+    sequences are packed token after token, Q as (total_q, Hq, d) and K, V as
+    (total_k, Hkv, d); sequence b owns query rows cu_q[b]..cu_q[b+1]-1 and keys
+    cu_k[b]..cu_k[b+1]-1 and attends only within itself. The causal alignment is
+    per sequence. A sequence with queries but no keys gives NaN rows (the same
+    reading as a row that sees no key).
 """
 from __future__ import annotations
 
@@ -196,3 +202,37 @@ def ulp_distance(a_bits, b_bits) -> np.ndarray:
         return np.where(x & 0x8000, -mag, mag)
 
     return np.abs(ordinal(a_bits) - ordinal(b_bits))
+
+
+def attention_varlen_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu_seqlens_q,
+                          cu_seqlens_k, scale: float, causal: bool = False) -> np.ndarray:
+    """Attention over a packed batch of variable-length sequences, in fp64.
+
+    The pages list variable-length ("varlen") batching among the features the
+    kernel lacks ([DK] "Hvad er udgivet" and "Autoregressiv serving, de praktiske
+    hager": production servers mix sequence lengths in one batch).
+
+    q: (total_q, Hq, d); k, v: (total_k, Hkv, d); cu_seqlens_q / cu_seqlens_k: B+1
+    non-decreasing offsets starting at 0 and ending at total_q / total_k. Each
+    sequence is one (1, S, H, d) problem for attention_fp64; the result has q's
+    shape. Rows of a sequence with no keys are NaN.
+    """
+    cq = [int(x) for x in cu_seqlens_q]
+    ck = [int(x) for x in cu_seqlens_k]
+    if len(cq) != len(ck) or cq[0] != 0 or ck[0] != 0:
+        raise ValueError("cu_seqlens must have B+1 entries starting at 0")
+    if any(b < a for a, b in zip(cq, cq[1:])) or any(b < a for a, b in zip(ck, ck[1:])):
+        raise ValueError("cu_seqlens must be non-decreasing")
+    if cq[-1] != q.shape[0] or ck[-1] != k.shape[0]:
+        raise ValueError("cu_seqlens must end at the packed lengths")
+    out = np.empty(q.shape, dtype=np.float64)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            out[q0:q1] = np.nan
+            continue
+        out[q0:q1] = attention_fp64(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], scale,
+                                    layout="bshd", causal=causal)[0]
+    return out

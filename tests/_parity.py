@@ -7,11 +7,12 @@ section "Numerik samlet eet sted", re-targeted at the exact fp64 result):
     rounding (same mode) of the exact value;
   * max |err| against the exact fp64 value <= 8e-3 for unit-normal inputs.
 
-Where an output's magnitude reaches 2 (causal rows that see only a few keys),
-one bf16 ULP exceeds 8e-3 and the correctly rounded RTZ value itself can miss
-the absolute bound. There the bound applies to the kernel's error beyond the one
-the rounding mode forces: |gpu - exact| - |oracle - exact| <= 8e-3
-("max_excess_err").
+Where an output's magnitude reaches 2 (causal rows or short sequences that see
+only a few keys), one bf16 ULP exceeds 8e-3: the correctly rounded RTZ value
+itself can miss the absolute bound, and so can any 1-ULP disagreement. There the
+bound applies to the elements more than 1 ULP from the oracle (the tail the 99.9%
+rule lets through), and to the kernel's error beyond the one the rounding mode
+forces: |gpu - exact| - |oracle - exact| <= 8e-3 ("max_excess_err").
 """
 from __future__ import annotations
 
@@ -50,7 +51,7 @@ def compare(gpu_bits: np.ndarray, exact: np.ndarray, mode: str) -> dict:
         "within_1ulp": float((d <= 1).mean()) if d.size else 1.0,
         "max_ulp": int(d.max()) if d.size else 0,
         "max_abs_err": float(err.max()) if err.size else 0.0,
-        "max_excess_err": float((err - forced).max()) if err.size else 0.0,
+        "max_excess_err": float((err - forced)[d > 1].max()) if (d > 1).any() else 0.0,
         "exact_match": float((d == 0).mean()) if d.size else 1.0,
     }
 

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for st in range(0, -11, -1):
+    for st in range(0, -12, -1):
         s = attn.status_str(st)
         assert s and s != "unknown status", st
     assert attn.status_str(-1234) == "unknown status"
@@ -132,6 +132,39 @@ def test_splitkv_valid_call_without_gpu_reports_no_device(lib):
 def test_ex_validation(lib, Hq, Hkv, flags, status):
     assert attn.attn_fwd_ex_raw(A, 2 * A, 3 * A, 4 * A, 0, 1, Hq, Hkv, 256, 256, 128, 0.088, 0,
                                 flags, 0) == status
+
+
+def _varlen(q=A, k=2 * A, v=3 * A, o=4 * A, cq=5 * A, ck=6 * A, B=2, Hq=4, Hkv=2, tq=300, tk=500,
+            maxq=200, d=128, scale=0.088, mode=0, flags=0):
+    return attn.attn_fwd_varlen_raw(q, k, v, o, cq, ck, B, Hq, Hkv, tq, tk, maxq, d, scale, mode,
+                                    flags, 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(cq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ck=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Hkv=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(tq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(tk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(maxq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(maxq=301), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(flags=4), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(mode=3), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(q=A + 8), attn.ATTN_ERR_MISALIGNED),
+    (dict(cq=5 * A + 2), attn.ATTN_ERR_MISALIGNED),
+    (dict(o=A), attn.ATTN_ERR_ALIASING),
+    (dict(o=5 * A - 256), attn.ATTN_ERR_ALIASING),   # out runs over cu_seqlens_q
+])
+def test_varlen_validation(lib, kw, status):
+    assert _varlen(**kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
+def test_varlen_valid_call_without_gpu_reports_no_device(lib):
+    assert _varlen(flags=attn.ATTN_FLAG_CAUSAL) == attn.ATTN_ERR_NO_DEVICE
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")

@@ -251,3 +251,125 @@ def test_gqa_equals_repeated_heads_and_sdpa():
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
     with pytest.raises(ValueError):
         attention_fp64(q, k[:, :1].repeat(4, axis=1), v[:, :1].repeat(4, axis=1), 0.1)
+
+
+# --- follow-on step: variable-length batches (packed tokens, cu_seqlens) ---------
+
+def _packed(lengths, H, seed):
+    total = int(sum(lengths))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return _rand((total, H, 128), seed), cu
+
+
+def _block_mask(cq, ck, causal):
+    """Allowed (query, key) pairs of the packed batch, built position by position."""
+    tq, tk = int(cq[-1]), int(ck[-1])
+    allowed = np.zeros((tq, tk), dtype=bool)
+    for b in range(len(cq) - 1):
+        for i in range(cq[b], cq[b + 1]):
+            for j in range(ck[b], ck[b + 1]):
+                li, lj = i - cq[b], j - ck[b]
+                lq, lk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+                allowed[i, j] = (not causal) or lj <= li + (lk - lq)
+    return allowed
+
+
+_VL_Q, _VL_K = [5, 1, 17, 9], [7, 3, 17, 2]
+
+
+def _varlen_pin(fn, causal):
+    """Compares fn (an attention_varlen_fp64) with torch SDPA over the whole packed
+    batch under an explicit block-diagonal mask; returns (matches, unseen rows)."""
+    q, cq = _packed(_VL_Q, 4, 60)
+    k, ck = _packed(_VL_K, 2, 61)
+    v, _ = _packed(_VL_K, 2, 62)
+    scale = inputs.default_scale()
+    got = fn(q, k, v, cq, ck, scale, causal=causal)
+    allowed = _block_mask(cq, ck, causal)
+    # The packed batch as one (1, H, T, d) problem; K/V heads repeated for the
+    # query heads that share them.
+    qt = np.swapaxes(q, 0, 1)[None]
+    kt = np.repeat(np.swapaxes(k, 0, 1)[None], 2, axis=1)
+    vt = np.repeat(np.swapaxes(v, 0, 1)[None], 2, axis=1)
+    want = np.swapaxes(_sdpa_mask(qt, kt, vt, float(np.float32(scale)), allowed)[0], 0, 1)
+    seen = allowed.any(axis=1)
+    ok = (np.allclose(got[seen], want[seen], rtol=1e-12, atol=1e-13)
+          and bool(np.isnan(got[~seen]).all()))
+    return ok, int((~seen).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_matches_sdpa_with_block_diagonal_mask(causal):
+    ok, unseen = _varlen_pin(oracle.attention_varlen_fp64, causal)
+    assert ok
+    # Causal: the last sequence has 9 queries and 2 keys, so its first 7 rows see
+    # no key and are NaN.
+    assert unseen == (7 if causal else 0)
+
+
+def _mutant_varlen(kind):
+    real = oracle.attention_fp64
+
+    def fn(q, k, v, cq, ck, scale, causal=False):
+        out = np.empty(q.shape)
+        for b in range(len(cq) - 1):
+            q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+            if kind == "key_offset_from_q":
+                k0, k1 = int(cq[b]), int(cq[b]) + (k1 - k0)
+            if kind == "key_off_by_one":
+                k1 = min(k1 + 1, k.shape[0])
+            if q1 == q0:
+                continue
+            if k1 <= k0:
+                out[q0:q1] = np.nan
+                continue
+            kk, vv = k[None, k0:k1], v[None, k0:k1]
+            if kind == "top_left_causal" and causal:
+                # causal aligned at the top left: query i sees keys 0..i
+                lq, lk = q1 - q0, k1 - k0
+                o = real(q[None, q0:q1], kk, vv, scale, layout="bshd")[0]
+                for i in range(lq):
+                    n = min(i + 1, lk)
+                    o[i] = real(q[None, q0 + i:q0 + i + 1], kk[:, :n], vv[:, :n], scale,
+                                layout="bshd")[0][0]
+                out[q0:q1] = o
+                continue
+            out[q0:q1] = real(q[None, q0:q1], kk, vv, scale, layout="bshd", causal=causal)[0]
+        return out
+    return fn
+
+
+@pytest.mark.parametrize("kind", ["key_offset_from_q", "key_off_by_one", "top_left_causal"])
+def test_varlen_planted_mistakes_are_caught(kind):
+    assert not _varlen_pin(_mutant_varlen(kind), causal=True)[0]
+    assert _varlen_pin(_mutant_varlen("none"), causal=True)[0]
+
+
+def test_varlen_sequence_order_does_not_matter():
+    lq, lk = [3, 8, 5], [4, 8, 6]
+    q, cq = _packed(lq, 2, 63)
+    k, ck = _packed(lk, 2, 64)
+    v, _ = _packed(lk, 2, 65)
+    got = oracle.attention_varlen_fp64(q, k, v, cq, ck, 0.1, causal=True)
+    order = [2, 0, 1]
+    def perm(x, cu):
+        return np.concatenate([x[cu[b]:cu[b + 1]] for b in order])
+    cq2 = np.concatenate([[0], np.cumsum([lq[b] for b in order])])
+    ck2 = np.concatenate([[0], np.cumsum([lk[b] for b in order])])
+    got2 = oracle.attention_varlen_fp64(perm(q, cq), perm(k, ck), perm(v, ck), cq2, ck2, 0.1,
+                                        causal=True)
+    assert (perm(got, cq) == got2).all()
+
+
+def test_varlen_empty_sequences():
+    q, cq = _packed([0, 4, 3], 1, 66)
+    k, ck = _packed([5, 0, 2], 1, 67)
+    v, _ = _packed([5, 0, 2], 1, 68)
+    got = oracle.attention_varlen_fp64(q, k, v, cq, ck, 0.1)
+    assert np.isnan(got[0:4]).all()          # sequence 1 has queries but no keys
+    # sequence 2 alone is ordinary attention of its 3 rows over its 2 keys
+    want = _sdpa(q[None, 4:7].swapaxes(1, 2), k[None, 5:7].swapaxes(1, 2),
+                 v[None, 5:7].swapaxes(1, 2), float(np.float32(0.1)))
+    np.testing.assert_allclose(got[4:7], want[0].swapaxes(0, 1), rtol=1e-12, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.attention_varlen_fp64(q, k, v, [0, 4, 3, 7], ck, 0.1)

@@ -25,3 +25,14 @@ def test_two_ulp_error_shows_as_excess():
     st = compare(bits, exact, "rtz")
     assert st["max_ulp"] == 2
     assert abs(st["max_excess_err"] - (2 * 2.0 ** -6 - 2.0 ** -9 - 2.0 ** -9)) < 1e-12
+
+
+def test_one_ulp_rtz_miss_at_a_grid_point_is_not_excess():
+    # Exact value just above 4.0; a kernel value just below 4.0 truncates one full
+    # ULP (2^-6) lower. Within 1 ULP, so no excess error although |err| > 8e-3.
+    exact = np.full(4, 4.0 + 2.0 ** -20)
+    bits = round_bf16(exact, "rtz")
+    bits[1] = round_bf16(np.array([4.0 - 2.0 ** -20]), "rtz")[0]
+    st = compare(bits, exact, "rtz")
+    assert st["max_ulp"] == 1 and st["max_abs_err"] > 8e-3
+    assert st["max_excess_err"] == 0.0
