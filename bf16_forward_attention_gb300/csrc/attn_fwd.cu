@@ -122,6 +122,16 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
 }
 
 int64_t kv_tiles_of(int64_t Sk) { return (Sk + attn::kBN - 1) / attn::kBN; }
+
+// Causal schedule: (batch, head) items per longest-first group, so that the K/V
+// of one group (512 bytes per key and head) take at most 48 MiB of the 126 MiB L2.
+int head_group_of(int64_t BH, int64_t keys_per_head) {
+  const int64_t per = 512 * (keys_per_head > 0 ? keys_per_head : 1);
+  int64_t g = (int64_t(48) << 20) / per;
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  return static_cast<int>(g);
+}
 int64_t qpairs_of(int64_t Sq) { return (Sq + 2 * attn::kBM - 1) / (2 * attn::kBM); }
 
 // Split workspace: unnormalised rows (128 fp32) then (reference max, row sum).
@@ -235,6 +245,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.cu_k = nullptr;
   p.max_sq = p.Sq;
   p.out = static_cast<uint16_t*>(out);
+  p.head_group = head_group_of(B * H, Sk);
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
@@ -359,6 +370,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
   p.cu_k = cu_seqlens_k;
   p.max_sq = static_cast<int>(max_seqlen_q);
   p.out = static_cast<uint16_t*>(out);
+  p.head_group = p.causal ? head_group_of(B * Hq, total_k / B) : 1;
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * Hq * n_qpairs);

@@ -111,6 +111,7 @@ struct Params {
   const int* cu_k;  // B + 1 key offsets
   int max_sq;       // bound on every sequence's query length (sizes the grid)
   uint16_t* out;    // output base, for rows stored without TMA
+  int head_group;   // causal: (batch, head) items scheduled together, longest first
 };
 
 // Bit 0: some wait timed out. Bit 1: a variable-length batch's offsets were
@@ -387,8 +388,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // The CTA's share of the work: (batch, head, query-tile pair, key split) and the
 // split's key tiles. Splits of one pair are adjacent in the grid, pairs of one
 // head are adjacent (so K/V of a head stay in L2); under the causal mask the
-// pairs go longest first over all heads instead, which balances the SMs' loads
-// (the blocks running at one time still share each head's K/V through L2).
+// pairs go longest first within groups of heads instead, which balances the
+// SMs' loads while the blocks running at one time share their heads' K/V
+// through L2.
 // Recomputed by each role where it is needed, rather than kept live across the
 // softmax loop.
 struct Work {
@@ -406,9 +408,17 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   w.split = blockIdx.x % p.n_splits;
   const int item = blockIdx.x / p.n_splits;
   if (kCausal || kVarlen) {
-    // Longest key ranges first over the whole grid (blocks start in index order).
-    w.pair = p.n_qpairs - 1 - item / p.BH;
-    w.bh = item % p.BH;
+    // Causal pairs differ in length: within each group of head_group (batch,
+    // head) items, longest key ranges first (blocks start in index order, so
+    // this is a greedy longest-first schedule); the group's K/V fit in L2. A
+    // variable-length batch without the mask uses groups of one item: the pairs
+    // of one (sequence, head) run together on its K/V.
+    const int span = p.n_qpairs * p.head_group;
+    const int g = item / span;
+    const int r = item - g * span;
+    const int gs = min(p.head_group, p.BH - g * p.head_group);
+    w.pair = p.n_qpairs - 1 - r / gs;
+    w.bh = g * p.head_group + r % gs;
   } else {
     w.pair = item % p.n_qpairs;
     w.bh = item / p.n_qpairs;
