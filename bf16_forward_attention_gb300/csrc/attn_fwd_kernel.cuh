@@ -64,6 +64,13 @@ constexpr uint32_t kRegsHigh = 232;  // each softmax warpgroup after the split
 static_assert(kRegsLow + 2 * kRegsHigh == 3 * kLaunchRegs, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (factor 256)
+// The tensor pipe accumulates P V over kFoldEvery key tiles in TMEM; then the
+// softmax threads fold that partial output into their fp32 registers (the
+// pipe's fp32 accumulation truncates, so a partial must not grow too long).
+// The split-KV variant, whose key ranges are short, folds every tile.
+constexpr int kFoldEvery = 4;
+template <bool kPartial>
+constexpr int kFoldOf = kPartial ? 1 : kFoldEvery;
 
 enum : int {
   kBarQ = 0,
@@ -188,7 +195,8 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_lo, uint32_t
   issue_s_seq(tmem_d, q_lo, k_lo, std::make_integer_sequence<int, 8>{});
 }
 
-// O_j = P_hi V_j + P_lo V_j into a fresh accumulator. P is in TMEM (A operand):
+// O += P_hi V_j + P_lo V_j, into a fresh accumulator unless `accumulate`. P is
+// in TMEM (A operand):
 // the 16 columns of key chunk u (keys 16u..16u+15) hold P_hi in their first 8
 // and P_lo in their last 8 columns, two bf16 per column. V_j (keys x head_dim,
 // head_dim contiguous) is the B operand in MN-major SW128: 8-key groups 1024 B
@@ -196,15 +204,18 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_lo, uint32_t
 // are 2048 bytes.
 template <int... kK>
 __device__ __forceinline__ void issue_pv_seq(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
+                                             uint32_t accumulate,
                                              std::integer_sequence<int, kK...>) {
   constexpr uint32_t idesc = idesc_bf16(kBM, kD, 1);
-  ((ptx::mma_ts_imm<16 * kK, (kK << 7)>(tmem_o, tmem_p, v_lo, kDescHi, idesc, kK == 0 ? 0u : 1u),
+  ((ptx::mma_ts_imm<16 * kK, (kK << 7)>(tmem_o, tmem_p, v_lo, kDescHi, idesc,
+                                         kK == 0 ? accumulate : 1u),
     ptx::mma_ts_imm<16 * kK + 8, (kK << 7)>(tmem_o, tmem_p, v_lo, kDescHi, idesc, 1u)),
    ...);
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo) {
-  issue_pv_seq(tmem_o, tmem_p, v_lo, std::make_integer_sequence<int, 8>{});
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
+                                         uint32_t accumulate) {
+  issue_pv_seq(tmem_o, tmem_p, v_lo, accumulate, std::make_integer_sequence<int, 8>{});
 }
 
 __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
@@ -367,6 +378,25 @@ __device__ __forceinline__ void rescale_row(Row& acc, float f) {
 }
 
 // acc += O (the last key tile's products; epilogue).
+// tO row *= f, 16 columns at a time (the stores complete before P_j is signalled).
+__device__ __forceinline__ void rescale_tmem_row(uint32_t tO, float f) {
+  const uint64_t f2 = ptx::f2_pack(f, f);
+#pragma unroll 1
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t r[16];
+    ptx::tmem_ld16(tO + 16 * ch, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float a, b;
+      ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), f2),
+                     a, b);
+      r[2 * i] = __float_as_uint(a);
+      r[2 * i + 1] = __float_as_uint(b);
+    }
+    ptx::tmem_st16(tO + 16 * ch, r);
+  }
+}
+
 __device__ __forceinline__ void fold_last(uint32_t tO, Row& acc) {
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
@@ -608,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = ring_wait(vit))) break;
           if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
           ptx::tc_fence_after();
-          issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit));
+          const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
+          issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
           if (!more) ptx::mma_commit(bar(kBarOFull + 0));
           if (more) {
             if (!(ok = ring_wait(kit))) break;
@@ -617,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
           ptx::tc_fence_after();
-          issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit));
+          issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
           ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
           if (!more) ptx::mma_commit(bar(kBarOFull + 1));
           if (more) {
@@ -682,26 +713,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
       // holds exactly that tile: the MMA that wrote S_j was issued after
       // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
-      float ext;
-      if (pos) {
-        if (j == 0) {
-          ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
-                       : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+      float ext, m_tile;
+      bool need;
+      if constexpr (kFoldOf<kPartial> == 1) {
+        if (pos) {
+          if (j == 0) {
+            ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                         : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+          } else {
+            ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                         : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+          }
         } else {
-          ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
-                       : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+          ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
+                       : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
+        }
+        m_tile = ext * c;
+        need = m_tile > m_used + kTau;  // false for NaN
+        if (need) {
+          const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+          if (j > 0) rescale_row(acc, f);
+          l *= f;
+          m_used = m_tile;
         }
       } else {
-        ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
-                     : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
-      }
-      const float m_tile = ext * c;
-      const bool need = m_tile > m_used + kTau;  // false for NaN
-      if (need) {
-        const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
-        if (j > 0) rescale_row(acc, f);
-        l *= f;
-        m_used = m_tile;
+        // The TMEM partial (key tiles since the last fold) is folded into the
+        // registers every kFoldOf<kPartial> tiles.
+        const bool fold_now = j > 0 && (j % kFoldOf<kPartial>) == 0;
+        if (pos) {
+          if (!fold_now) {
+            ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                         : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+          } else {
+            ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                         : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+          }
+        } else {
+          ext = masked ? fold_and_min<true>(tS, tO, acc, valid, fold_now)
+                       : fold_and_min<false>(tS, tO, acc, kBN, fold_now);
+        }
+        m_tile = ext * c;
+        need = m_tile > m_used + kTau;  // false for NaN
+        float f_row = 1.f;  // this row's rescale factor at this tile
+        if (need) {
+          const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+          if (j > 0) rescale_row(acc, f);
+          l *= f;
+          m_used = m_tile;
+          f_row = f;
+        }
+        // A partial still in TMEM is relative to the old reference: scale it in
+        // place (the PV MMAs that wrote it are done, S_j being ready; the next one
+        // waits for P_j). Warp-uniform: each lane rescales its own row, by 1 if its
+        // reference did not move.
+        if ((j % kFoldOf<kPartial>) != 0 && __any_sync(0xFFFFFFFFu, need))
+          rescale_tmem_row(tO, f_row);
       }
       const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
       // Causal, c > 0: pass A left -Inf in the hidden columns, so pass B needs
