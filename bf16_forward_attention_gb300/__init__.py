@@ -85,6 +85,12 @@ def load_library() -> ctypes.CDLL:
     lib.attn_fwd_varlen.argtypes = ([ctypes.c_void_p] * 6 + [i64] * 7
                                     + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p])
     lib.attn_fwd_varlen.restype = ctypes.c_int
+    lib.attn_fwd_host_workspace_bytes.argtypes = [i64] * 6
+    lib.attn_fwd_host_workspace_bytes.restype = i64
+    lib.attn_fwd_host.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] + [i64] * 6
+                                  + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, i64,
+                                     ctypes.c_void_p])
+    lib.attn_fwd_host.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -280,6 +286,62 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, *,
     return out
 
 
+def host_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, d: int = 128) -> int:
+    """Device workspace attn_fwd_host needs (negative: a status code)."""
+    return load_library().attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, d)
+
+
+def attn_fwd_host_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, B: int,
+                      Hq: int, Hkv: int, Sq: int, Sk: int, d: int, scale: float,
+                      rounding_mode: int, flags: int, workspace_ptr: int, workspace_bytes: int,
+                      stream: int) -> int:
+    """Direct call of ``attn_fwd_host`` (host buffers, copies overlapped)."""
+    return load_library().attn_fwd_host(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, Hq, Hkv, Sq, Sk,
+                                        d, ctypes.c_float(scale), rounding_mode, flags,
+                                        workspace_ptr, workspace_bytes, stream)
+
+
+def attn_fwd_host(q, k, v, *, causal: bool = False, layout: str = "bhsd",
+                  scale: float | None = None, rounding: str = "rtne", out=None, workspace=None,
+                  device=None):
+    """attn_fwd_ex on CPU tensors (pinned for overlap): uploads, computes and
+    downloads in overlapped chunks on ``device`` and returns ``out`` (a CPU
+    tensor, pinned when allocated here). The call is asynchronous on the
+    current stream: synchronize before reading ``out``."""
+    import torch
+
+    if layout not in LAYOUTS or rounding not in ROUNDINGS:
+        raise ValueError("unknown layout or rounding mode")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CPU tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, Hq, Sq, D = _dims(q, layout)
+    Bk, Hkv, Sk, Dk = _dims(k, layout)
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    need = host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D)
+    if need < 0:
+        raise AttnError(need, status_str(need))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(device):
+        stream = torch.cuda.current_stream(device).cuda_stream
+        st = attn_fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               LAYOUTS[layout], B, Hq, Hkv, Sq, Sk, D, float(scale),
+                               ROUNDINGS[rounding], ATTN_FLAG_CAUSAL if causal else 0,
+                               workspace.data_ptr(), workspace.numel(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, status_str(st))
+    return out
+
+
 def attn_fwd_last_error() -> int:
     return load_library().attn_fwd_last_error()
 
@@ -337,5 +399,6 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
 __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_selftest_raw",
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
            "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw",
-           "attn_fwd_varlen", "attn_fwd_varlen_raw", "ATTN_ERR_SEQLENS", "status_str", "load_library",
+           "attn_fwd_varlen", "attn_fwd_varlen_raw", "ATTN_ERR_SEQLENS",
+           "attn_fwd_host", "attn_fwd_host_raw", "host_workspace_bytes", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]

@@ -2,8 +2,9 @@
 
     python -m bf16_forward_attention_gb300.build [--force]
 
-One translation unit, one -gencode; the CUDA runtime is linked statically and the
-driver's tensor-map encoder is looked up at run time, so the library loads (and
+Two translation units (the kernels with their launcher, and the host-buffer
+pipeline), one -gencode; the CUDA runtime is linked statically and the driver's
+tensor-map encoder is looked up at run time, so the library loads (and
 reports ATTN_ERR_NO_DEVICE) on a machine without a GPU.
 """
 from __future__ import annotations
@@ -19,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libattn_fwd.so")
-SOURCES = [os.path.join(CSRC, "attn_fwd.cu")]
+SOURCES = [os.path.join(CSRC, "attn_fwd.cu"), os.path.join(CSRC, "attn_host.cu")]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

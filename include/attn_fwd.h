@@ -207,6 +207,38 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
 const char* attn_status_str(int status);
 
 /*
+ * attn_fwd_host - attn_fwd_ex on HOST buffers, with the copies overlapped.
+ * The pages measure the kernel alone; a caller that holds its tensors in host
+ * memory pays for the copies too, and this entry hides most of them behind
+ * the kernel. It has no counterpart on the pages.
+ *
+ *   q, k, v, out   host memory, in `layout`, sizes as attn_fwd_ex (out written).
+ *                  Page-locked memory (cudaHostAlloc / cudaHostRegister) lets
+ *                  the copies run asynchronously and overlap the kernels;
+ *                  pageable memory works but the copies then serialise.
+ *   workspace      device memory of attn_fwd_host_workspace_bytes() bytes,
+ *                  256-byte aligned, owned by the caller; it receives copies of
+ *                  q, k, v and out in the same layout. Calls in flight at the
+ *                  same time need separate workspaces.
+ *   stream         the call is ordered after the work already on `stream`, and
+ *                  later work on `stream` is ordered after all of it: `out` is
+ *                  valid once `stream` has reached this point.
+ * The problem is cut into up to 8 chunks that are contiguous in every tensor
+ * (runs of heads for BHSD, runs of batch entries or of query rows for BSHD);
+ * each chunk's upload, kernel (attn_fwd_ex on the sub-tensors) and download
+ * run on internal streams ordered by events, so chunk i's kernel overlaps the
+ * copies of its neighbours. Results are bit-identical to attn_fwd_ex.
+ * Errors: as attn_fwd_ex, and ATTN_ERR_INVALID_ARG for a missing or short
+ * workspace, ATTN_ERR_MISALIGNED for a workspace not 256-byte aligned.
+ */
+int64_t attn_fwd_host_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk,
+                                      int64_t d);
+int attn_fwd_host(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
+                  int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                  int rounding_mode, int flags, void* workspace, int64_t workspace_bytes,
+                  void* stream);
+
+/*
  * Device-side status of earlier launches on the current device: ATTN_OK;
  * ATTN_ERR_TIMEOUT if some launch gave up on a wait that did not finish within
  * its time limit (the kernel then stops its work, waits for its own copies in

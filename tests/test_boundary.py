@@ -167,6 +167,41 @@ def test_varlen_valid_call_without_gpu_reports_no_device(lib):
     assert _varlen(flags=attn.ATTN_FLAG_CAUSAL) == attn.ATTN_ERR_NO_DEVICE
 
 
+def _host(q=A, k=2 * A, v=3 * A, o=4 * A, layout=1, B=2, Hq=16, Hkv=16, Sq=8192, Sk=8192, d=128,
+          scale=0.088, mode=0, flags=0, ws=8 * A, wsb=None):
+    need = attn.host_workspace_bytes(B, Hq, Hkv, Sq, Sk, d) if wsb is None else wsb
+    return attn.attn_fwd_host_raw(q, k, v, o, layout, B, Hq, Hkv, Sq, Sk, d, scale, mode, flags, ws,
+                                  max(need, 0), 0)
+
+
+def test_host_buffer_workspace_bytes(lib):
+    assert attn.host_workspace_bytes(2, 16, 4, 8192, 1000) == 2 * 2 * 16 * 8192 * 256 + 2 * 2 * 4 * 1000 * 256
+    assert attn.host_workspace_bytes(1, 1, 1, 1, 1) == 4 * 256
+    assert attn.host_workspace_bytes(1, 6, 4, 10, 10) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.host_workspace_bytes(1, 2, 2, 10, 10, 64) == attn.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(wsb=1000), attn.ATTN_ERR_INVALID_ARG),       # workspace too small
+    (dict(Hkv=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(flags=2), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(layout=5), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(mode=7), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=8 * A + 16), attn.ATTN_ERR_MISALIGNED),    # workspace must be 256-byte aligned
+])
+def test_host_buffer_validation(lib, kw, status):
+    assert _host(**kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
+def test_host_buffer_call_without_gpu_reports_no_device(lib):
+    assert _host(flags=attn.ATTN_FLAG_CAUSAL) == attn.ATTN_ERR_NO_DEVICE
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
 def test_ex_valid_call_without_gpu_reports_no_device(lib):
     assert attn.attn_fwd_ex_raw(A, 2 * A, 3 * A, 4 * A, 1, 1, 8, 2, 256, 300, 128, 0.088, 0,
