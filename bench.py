@@ -237,9 +237,13 @@ def run_reference(args, w):
     from bf16_forward_attention_gb300 import inputs
 
     q, k, v = inputs.make_qkv(w)
+    # Each step is a bounded sample of the workload; the whole run stays near
+    # 150 s of CPU work whatever --steps and --warmup are.
+    n = max(1, args.warmup + args.steps)
+    step_s = args.ref_step_seconds if args.ref_step_seconds else min(10.0, max(0.5, 150.0 / n))
     done = []
     for i in range(args.warmup + args.steps):
-        f, t, rows = _cpu_sample(w, q, k, v, budget_s=args.ref_step_seconds)
+        f, t, rows = _cpu_sample(w, q, k, v, budget_s=step_s)
         if i >= args.warmup:
             done.append((f, t, rows))
     t_total = sum(t for _, t, _ in done)
@@ -252,7 +256,7 @@ def run_reference(args, w):
         "data": "synthetic", "config": _config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
                          "sample": f"{rows} query rows of the workload, each against {_keys_seen(w)} "
-                                   f"(~{args.ref_step_seconds:g} s of fp64 CPU work per step)"},
+                                   f"(~{step_s:.2g} s of fp64 CPU work per step)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -457,7 +461,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="self8k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=None,
+                    help="fp64 CPU seconds per reference step (default: a 150 s budget for "
+                         "the whole run over warmup + steps, 0.5..10 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the kernel, from an ncu capture")
