@@ -240,7 +240,6 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.withhold_s0 = withhold_s0;
   p.group = static_cast<int>(H / Hkv);
   p.causal = causal ? 1 : 0;
-  p.causal_off = static_cast<int>(Sk - Sq);
   p.cu_q = nullptr;
   p.cu_k = nullptr;
   p.max_sq = p.Sq;
@@ -365,7 +364,6 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
   p.withhold_s0 = 0;
   p.group = static_cast<int>(Hq / Hkv);
   p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
-  p.causal_off = 0;
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
   p.max_sq = static_cast<int>(max_seqlen_q);

@@ -32,9 +32,10 @@
 //
 // The tensor pipe's fp32 accumulation truncates; summed over tens of thousands
 // of keys that bias costs ~0.3% (32K keys) to ~1.5% (128K keys) of outputs their
-// 1-ULP bound. So the PV products of each key tile go into a fresh TMEM
-// accumulator (16 MMAs deep), and each softmax thread adds it into its row's 128
-// fp32 registers, rounding to nearest, before it hands over the next P.
+// 1-ULP bound. So the PV products accumulate in TMEM over at most kFoldEvery
+// key tiles (64 MMAs deep), after which each softmax thread adds that partial
+// into its row's 128 fp32 registers, rounding to nearest, and the next partial
+// starts fresh.
 //
 // Every wait is bounded in time. A wait that expires sets a device status word,
 // raises a CTA-wide abort flag, and every role then stops, waits for its own
@@ -110,8 +111,7 @@ struct Params {
   unsigned long long timeout_ns;
   int withhold_s0;  // self-test of the timeout path: never signal query tile 0's first S
   int group;        // query heads per key/value head (grouped-query attention)
-  int causal;       // 1: key j visible to query i iff j <= i + causal_off
-  int causal_off;   // Sk - Sq
+  int causal;       // 1: key j visible to query i iff j <= i + Sk - Sq (per sequence)
   // Variable-length batch (packed tokens; the tensor maps then have B = 1 and
   // S = total tokens, and B above is the number of sequences):
   const int* cu_q;  // B + 1 query offsets (device memory)
@@ -426,7 +426,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 struct Work {
   int split, pair, bh, head, kv_head, batch;
   int tile0, n_kv;  // key tiles [tile0, tile0 + n_kv)
-  bool has_tail;    // this split holds the ragged last key tile
   int q_base, k_base;  // first query / key token of the sequence (varlen; else 0)
   int sq, sk;          // the sequence's query / key lengths
   bool bad;            // varlen: the offsets of this sequence are invalid
@@ -487,7 +486,6 @@ __device__ __forceinline__ Work work_of(const Params& p) {
     const int tiles = visible <= 0 ? 1 : (visible + kBN - 1) / kBN;
     w.n_kv = min(tiles, kv_tiles);
   }
-  w.has_tail = w.tile0 + w.n_kv == p.kv_tiles && p.kv_tail < kBN;
   return w;
 }
 
@@ -710,9 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int valid = kRowLimit ? row_lim - kBN * j : p.kv_tail;
       // Least `valid` over the warp (lane 0 has the warp's first row).
       const int vmin = kRowLimit ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
-      // Pass A: fold key tile j-1's products into the row (the TMEM accumulator
-      // holds exactly that tile: the MMA that wrote S_j was issued after
-      // PV_{j-1}, and PV_j waits for P_j), and take the row extreme of S_j.
+      // Pass A: take the row extreme of S_j and, on a fold tile, add the TMEM
+      // partial into the row (it holds the tiles since the last fold, complete
+      // because the MMA that wrote S_j was issued after PV_{j-1}, and PV_j waits
+      // for P_j).
       float ext, m_tile;
       bool need;
       if constexpr (kFoldOf<kPartial> == 1) {
