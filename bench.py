@@ -56,14 +56,27 @@ KERNEL_SOURCES = ("bf16_forward_attention_gb300/csrc/attn_fwd_kernel.cuh",
                   "bf16_forward_attention_gb300/csrc/attn_fwd.cu")
 
 
+def kernel_sources_hash() -> str:
+    """sha256 (16 hex) of the kernel sources with comments and whitespace removed,
+    so that only a change that can alter the compiled kernel makes it differ."""
+    import hashlib
+    import re
+
+    code = []
+    for p in KERNEL_SOURCES:
+        text = open(os.path.join(ROOT, p)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        code.append(" ".join(text.split()))
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
+
+
 def _recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu record, if it was taken on
-    exactly the current kernel sources (else None: the counters are stale)."""
-    import hashlib
+    the current kernel code (else None: the counters are stale)."""
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["attn_fwd_kernel"][workload]
-        h = hashlib.sha256(b"".join(open(os.path.join(ROOT, p), "rb").read()
-                                    for p in KERNEL_SOURCES)).hexdigest()[:16]
+        h = kernel_sources_hash()
     except (OSError, KeyError, ValueError):
         return None
     return float(rec["dram_bytes_per_launch"]) if rec.get("sources_sha256_16") == h else None
