@@ -172,13 +172,17 @@ def attn_fwd_splitkv(q, k, v, *, num_splits: int | None = None, layout: str = "b
     Bk, Hk, Sk, Dk = _dims(k, layout)
     if (Bk, Hk, Dk) != (B, H, D) or tuple(v.shape) != tuple(k.shape):
         raise ValueError("shape mismatch")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
     if num_splits is None:
         num_splits = splitkv_num_splits(B, H, Sq, Sk)
     need = splitkv_workspace_bytes(B, H, Sq, Sk, num_splits, D)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_workspace(workspace, q.device)
     if out is None:
         out = torch.empty_like(q)
+    _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
@@ -217,8 +221,11 @@ def attn_fwd_ex(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     Bk, Hkv, Sk, Dk = _dims(k, layout)
     if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
         raise ValueError("shape mismatch")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
     if out is None:
         out = torch.empty_like(q)
+    _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
@@ -270,8 +277,11 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, *,
     total_k, Hkv, Dk = k.shape
     if Dk != D or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
         raise ValueError("shape mismatch")
+    if not (q.device == k.device == v.device == cu_seqlens_q.device == cu_seqlens_k.device):
+        raise ValueError("q, k, v and the offsets must be on one device")
     if out is None:
         out = torch.empty_like(q)
+    _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
@@ -307,7 +317,8 @@ def attn_fwd_host(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     """attn_fwd_ex on CPU tensors (pinned for overlap): uploads, computes and
     downloads in overlapped chunks on ``device`` and returns ``out`` (a CPU
     tensor, pinned when allocated here). The call is asynchronous on the
-    current stream: synchronize before reading ``out``."""
+    current stream: synchronize before reading ``out``, and keep q, k, v (and a
+    caller-given workspace) alive until then."""
     import torch
 
     if layout not in LAYOUTS or rounding not in ROUNDINGS:
@@ -321,14 +332,18 @@ def attn_fwd_host(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     Bk, Hkv, Sk, Dk = _dims(k, layout)
     if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
         raise ValueError("shape mismatch")
+    if out is not None:
+        _check_out(out, q)
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     need = host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D)
     if need < 0:
         raise AttnError(need, status_str(need))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    _check_workspace(workspace, torch.device(device))
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(device):
@@ -352,6 +367,23 @@ def _dims(x, layout):
     else:
         B, S, H, D = x.shape
     return B, H, S, D
+
+
+def _check_out(out, q):
+    """The C library writes through out's pointer: it must be a contiguous bf16
+    tensor shaped like q, on q's device (CUDA or host)."""
+    import torch
+
+    if (not isinstance(out, torch.Tensor) or out.dtype != torch.bfloat16
+            or out.shape != q.shape or not out.is_contiguous() or out.device != q.device):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
+
+
+def _check_workspace(ws, device):
+    import torch
+
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous CUDA tensor on {device}")
 
 
 def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,

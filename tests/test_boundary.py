@@ -221,6 +221,16 @@ def test_python_binding_checks(lib):
         attn.attn_fwd(x, x, x, layout="sbhd")
     with pytest.raises(ValueError):
         attn.attn_fwd(x, x, x, rounding="rtp")
+    # attn_fwd_host takes host tensors; a wrongly shaped or typed out is refused
+    # before the library writes through its pointer.
+    with pytest.raises(ValueError):
+        attn.attn_fwd_host(x, x, x, out=torch.zeros(1, 1, 3, 128, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        attn.attn_fwd_host(x, x, x, out=torch.zeros(1, 1, 4, 128, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        attn.attn_fwd_host(x, x[:, :, :2].repeat(1, 2, 1, 1)[:, :1], x)  # k, v shapes differ
+    with pytest.raises(TypeError):
+        attn.attn_fwd_host(x.float(), x, x)
 
 
 def test_product_package_does_not_import_oracle():
