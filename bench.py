@@ -210,6 +210,31 @@ def _cpu_sample_varlen(w, q, k, v, budget_s, scale):
     return 4.0 * pairs * w.D, t_used, rows_done
 
 
+def _env_record(dev):
+    """Versions and GPU state the numbers were taken with."""
+    import subprocess
+
+    def run(cmd):
+        try:
+            return subprocess.run(cmd, capture_output=True, text=True, timeout=20,
+                                  cwd=ROOT).stdout.strip() or None
+        except (OSError, subprocess.SubprocessError):
+            return None
+
+    props = torch.cuda.get_device_properties(dev)
+    nvcc = run(["nvcc", "--version"])
+    return {
+        "git": run(["git", "rev-parse", "--short", "HEAD"]),
+        "torch": torch.__version__, "cuda_runtime": torch.version.cuda,
+        "nvcc": nvcc.splitlines()[-1] if nvcc else None,
+        "driver": run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                       "-i", str(dev.index or 0)]),
+        "sm_count": props.multi_processor_count,
+        "compute_capability": f"{props.major}.{props.minor}",
+        "kernel_code_hash": kernel_sources_hash(),
+    }
+
+
 def _keys_seen(w):
     return f"its visible keys of {w.Sk} (causal)" if w.causal else f"all {w.Sk} keys"
 
@@ -459,6 +484,7 @@ def run_ours(args, w):
         "splits": splits,
         "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
+        "env": _env_record(dev),
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -12,7 +12,7 @@ import ctypes
 import math
 import os
 
-from .build import LIB_PATH
+from .build import lib_path
 
 LAYOUTS = {"bhsd": 0, "bshd": 1}
 ROUNDINGS = {"rtne": 0, "rtna": 1, "rtz": 2}
@@ -29,9 +29,10 @@ ATTN_ERR_TIMEOUT = -8
 ATTN_ERR_TOO_LARGE = -9
 ATTN_ERR_SCRATCH = -10
 ATTN_ERR_SEQLENS = -11
+ATTN_ERR_DEBUG_CHECK = -12
 ATTN_FLAG_CAUSAL = 1
 
-_lib = None
+_libs: dict = {}
 
 
 class AttnError(RuntimeError):
@@ -42,16 +43,20 @@ class AttnError(RuntimeError):
         self.status = status
 
 
-def load_library() -> ctypes.CDLL:
-    """Load ``libattn_fwd.so`` (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
+def load_library(debug: bool | None = None) -> ctypes.CDLL:
+    """Load ``libattn_fwd.so``, or its debug flavour ``libattn_fwd_debug.so`` when
+    ``debug`` (default: the environment variable ATTN_FWD_DEBUG=1). Raises if the
+    library has not been built."""
+    if debug is None:
+        debug = os.environ.get("ATTN_FWD_DEBUG") == "1"
+    if debug in _libs:
+        return _libs[debug]
+    path = lib_path(debug)
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"CUDA library not built: {LIB_PATH} is missing. "
-            "Run `python -m bf16_forward_attention_gb300.build` (needs nvcc).")
-    lib = ctypes.CDLL(LIB_PATH)
+            f"CUDA library not built: {path} is missing. Run "
+            f"`python -m bf16_forward_attention_gb300.build{' --debug' if debug else ''}` (needs nvcc).")
+    lib = ctypes.CDLL(path)
     i64 = ctypes.c_int64
     lib.attn_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64, i64, i64,
                                                      ctypes.c_float, ctypes.c_int, ctypes.c_void_p]
@@ -91,7 +96,11 @@ def load_library() -> ctypes.CDLL:
                                   + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, i64,
                                      ctypes.c_void_p])
     lib.attn_fwd_host.restype = ctypes.c_int
-    _lib = lib
+    lib.attn_fwd_debug_build.argtypes = []
+    lib.attn_fwd_debug_build.restype = ctypes.c_int
+    lib.attn_fwd_debug_selftest.argtypes = lib.attn_fwd.argtypes
+    lib.attn_fwd_debug_selftest.restype = ctypes.c_int
+    _libs[debug] = lib
     return lib
 
 
@@ -433,4 +442,4 @@ __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_
            "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw",
            "attn_fwd_varlen", "attn_fwd_varlen_raw", "ATTN_ERR_SEQLENS",
            "attn_fwd_host", "attn_fwd_host_raw", "host_workspace_bytes", "status_str", "load_library",
-           "AttnError", "LAYOUTS", "ROUNDINGS", "LIB_PATH"]
+           "AttnError", "LAYOUTS", "ROUNDINGS", "lib_path", "ATTN_ERR_DEBUG_CHECK"]

@@ -158,6 +158,7 @@ const char* attn_status_str(int status) {
     case ATTN_ERR_TOO_LARGE: return "size beyond tensor-map or grid limits";
     case ATTN_ERR_SCRATCH: return "split workspace needed exceeds the library's fixed 32 MiB device scratch";
     case ATTN_ERR_SEQLENS: return "invalid cu_seqlens contents (found on the device; those sequences were not computed)";
+    case ATTN_ERR_DEBUG_CHECK: return "a bounds or protocol check of the debug build failed (the access it guards was skipped)";
     default: return "unknown status";
   }
 }
@@ -171,7 +172,8 @@ namespace {
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
                   int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
                   void* stream, unsigned long long timeout_ns, int withhold_s0, int n_splits,
-                  void* workspace, int64_t workspace_bytes, int64_t Hkv = 0, int causal = 0) {
+                  void* workspace, int64_t workspace_bytes, int64_t Hkv = 0, int causal = 0,
+                  int dbg_poison = 0) {
   if (Hkv == 0) Hkv = H;
   // ---- host-side validation (nothing is launched on failure)
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
@@ -245,6 +247,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.max_sq = p.Sq;
   p.out = static_cast<uint16_t*>(out);
   p.head_group = head_group_of(B * H, Sk);
+  p.dbg_poison = dbg_poison;
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
@@ -369,6 +372,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
   p.max_sq = static_cast<int>(max_seqlen_q);
   p.out = static_cast<uint16_t*>(out);
   p.head_group = p.causal ? head_group_of(B * Hq, total_k / B) : 1;
+  p.dbg_poison = 0;
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * Hq * n_qpairs);
@@ -427,6 +431,16 @@ int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void*
                        timeout_ns, 1, 1, nullptr, 0);
 }
 
+int attn_fwd_debug_build(void) { return ATTN_DEBUG ? 1 : 0; }
+
+int attn_fwd_debug_selftest(const void* q, const void* k, const void* v, void* out, int layout,
+                            int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                            int rounding_mode, void* stream) {
+  if (!ATTN_DEBUG) return ATTN_ERR_UNSUPPORTED;
+  return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
+                       kTimeoutNs, 0, 1, nullptr, 0, 0, 0, 1);
+}
+
 int attn_fwd_last_error(void) {
   unsigned int s = 0;
   if (cudaMemcpyFromSymbol(&s, attn::g_attn_status, sizeof(s)) != cudaSuccess) {
@@ -436,7 +450,8 @@ int attn_fwd_last_error(void) {
   if (s == 0) return ATTN_OK;
   const unsigned int zero = 0;
   cudaMemcpyToSymbol(attn::g_attn_status, &zero, sizeof(zero));
-  return (s & 1u) ? ATTN_ERR_TIMEOUT : ATTN_ERR_SEQLENS;
+  if (s & 1u) return ATTN_ERR_TIMEOUT;
+  return (s & 2u) ? ATTN_ERR_SEQLENS : ATTN_ERR_DEBUG_CHECK;
 }
 
 }  // extern "C"

@@ -119,11 +119,30 @@ struct Params {
   int max_sq;       // bound on every sequence's query length (sizes the grid)
   uint16_t* out;    // output base, for rows stored without TMA
   int head_group;   // causal: (batch, head) items scheduled together, longest first
+  int dbg_poison;   // debug build only: report one failed check (tests the reporting)
 };
 
 // Bit 0: some wait timed out. Bit 1: a variable-length batch's offsets were
-// invalid (that sequence's output is left unwritten).
+// invalid (that sequence's output is left unwritten). Bit 2 (debug build): a
+// bounds or protocol check failed.
 __device__ unsigned int g_attn_status;
+
+// Debug build (-DATTN_DEBUG=1): dbg_ok(cond) records a failed check in bit 2 of
+// the status word and returns cond, so that the caller can skip the access it
+// guards; no trap, no assert. In the release build it is the constant true and
+// the checks compile away.
+#ifndef ATTN_DEBUG
+#define ATTN_DEBUG 0
+#endif
+__device__ __forceinline__ bool dbg_ok(bool cond) {
+#if ATTN_DEBUG
+  if (!cond) atomicOr(&g_attn_status, 4u);
+  return cond;
+#else
+  (void)cond;
+  return true;
+#endif
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start,
 // leading and stride byte offsets in 16-byte units, version 1, layout 2). Every
@@ -527,6 +546,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (2 * kBM * wk.pair >= wk.sq) return;
   }
+#if ATTN_DEBUG
+  if (threadIdx.x == 0) {
+    if (p.dbg_poison) dbg_ok(false);
+    const Work wk = work_of<kCausal, kVarlen>(p);
+    dbg_ok(wk.pair >= 0 && wk.pair < p.n_qpairs && wk.bh >= 0 && wk.bh < p.BH && wk.n_kv >= 1 &&
+           wk.kv_head >= 0 && wk.kv_head * p.group < p.H);
+    dbg_ok(kVarlen || wk.tile0 + wk.n_kv <= p.kv_tiles);
+  }
+#endif
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(kBarQ), 1);
@@ -571,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv_head = wk.kv_head, q_base = wk.q_base, k_base = wk.k_base;
         int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
         int c1, c2;
+        dbg_ok(q_base + 2 * pair * kBM < p.Sq);  // the first query tile starts inside
         ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
         for (int t = 0; t < kQTiles; ++t) {
           tma_coords(p.layout, q_base + (2 * pair + t) * kBM, head, c1, c2);
@@ -583,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t parity = ((it / kStages) & 1) ^ 1;
           if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
           const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+          dbg_ok(k_base + (tile0 + (it >> 1)) * kBN < p.Sk + kBN);
           tma_coords(p.layout, k_base + (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
           ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
@@ -593,6 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Let every copy this thread started land before the CTA can exit. On
         // the normal path these phases have long completed; after an abort the
         // consumer may never have waited for them.
+        dbg_ok(issued == 2 * n_kv || *abort_flag);  // every fill of the plan was issued
         wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
         for (int s = 0; s < kStages && s < issued; ++s) {
           const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
@@ -789,17 +820,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q = (2 * wk.pair + t) * kBM + row;
       if (q < p.Sq) {
         const size_t r = (static_cast<size_t>(wk.split) * p.BH + wk.bh) * p.sq_pad + q;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + r * kD);
+        if (dbg_ok(r < static_cast<size_t>(p.n_splits) * p.BH * p.sq_pad)) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + r * kD);
 #pragma unroll
-        for (int i = 0; i < kD / 4; ++i) {
-          float a0, a1, a2, a3;
-          ptx::f2_unpack(acc[2 * i], a0, a1);
-          ptx::f2_unpack(acc[2 * i + 1], a2, a3);
-          dst[i] = make_float4(a0, a1, a2, a3);
+          for (int i = 0; i < kD / 4; ++i) {
+            float a0, a1, a2, a3;
+            ptx::f2_unpack(acc[2 * i], a0, a1);
+            ptx::f2_unpack(acc[2 * i + 1], a2, a3);
+            dst[i] = make_float4(a0, a1, a2, a3);
+          }
+          // The products are relative to m_used, or to 0 while it is -Inf (then no
+          // key had a finite logit and both sums are 0, or NaN).
+          reinterpret_cast<float2*>(p.part_rl)[r] = make_float2(m_used, l);
         }
-        // The products are relative to m_used, or to 0 while it is -Inf (then no key
-        // had a finite logit and both sums are 0, or NaN).
-        reinterpret_cast<float2*>(p.part_rl)[r] = make_float2(m_used, l);
       }
     } else if (ok) {
       ptx::tc_fence_after();
@@ -831,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;  // within the sequence
       if (!kVarlen || q_row0 + 32 <= wk.sq) {
-        if (lane == 0 && q_row0 < wk.sq) {
+        if (lane == 0 && q_row0 < wk.sq && dbg_ok(wk.q_base + q_row0 < p.Sq)) {
           int c1, c2;
           tma_coords(p.layout, wk.q_base + q_row0, wk.head, c1, c2);
           for (int hf = 0; hf < 2; ++hf)
@@ -840,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::bulk_commit_group();
           ptx::bulk_wait_group_0();
         }
-      } else if (lane < wk.sq - q_row0) {
+      } else if (lane < wk.sq - q_row0 && dbg_ok(wk.q_base + q_row0 + lane < p.Sq)) {
         // The sequence ends inside this warp's rows: a TMA box would run into the
         // next sequence's rows, so each row up to the end is copied out of the
         // staging buffer with plain 16-byte stores (packed layout: token, head).

@@ -53,8 +53,10 @@ enum {
   ATTN_ERR_TIMEOUT = -8,     /* a bounded device-side wait expired             */
   ATTN_ERR_TOO_LARGE = -9,   /* a size beyond the tensor-map / grid limits     */
   ATTN_ERR_SCRATCH = -10,    /* attn_fwd_splitkv_noalloc: workspace > 32 MiB   */
-  ATTN_ERR_SEQLENS = -11     /* attn_fwd_varlen: invalid offsets, found on the
+  ATTN_ERR_SEQLENS = -11,    /* attn_fwd_varlen: invalid offsets, found on the
                                 device and reported by attn_fwd_last_error     */
+  ATTN_ERR_DEBUG_CHECK = -12 /* debug build: a bounds or protocol check failed,
+                                reported by attn_fwd_last_error                */
 };
 
 /*
@@ -239,11 +241,29 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* out, int la
                   void* stream);
 
 /*
+ * Debug build. The library built with -DATTN_DEBUG=1 (libattn_fwd_debug.so)
+ * checks, inside the kernel, every computed tile coordinate, global row index
+ * and the producer's count of ring fills; a failed check skips the access it
+ * guards and raises a status that attn_fwd_last_error() returns as
+ * ATTN_ERR_DEBUG_CHECK (no trap, no assert). It has no counterpart on the pages.
+ *   attn_fwd_debug_build()     1 in the debug build, 0 in the release build
+ *   attn_fwd_debug_selftest()  debug build: an attn_fwd launch (same arguments)
+ *                              whose first thread reports one failed check
+ *                              without any bad access, to test the reporting;
+ *                              release build: ATTN_ERR_UNSUPPORTED, no launch
+ */
+int attn_fwd_debug_build(void);
+int attn_fwd_debug_selftest(const void* q, const void* k, const void* v, void* out, int layout,
+                            int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
+                            int rounding_mode, void* stream);
+
+/*
  * Device-side status of earlier launches on the current device: ATTN_OK;
  * ATTN_ERR_TIMEOUT if some launch gave up on a wait that did not finish within
  * its time limit (the kernel then stops its work, waits for its own copies in
  * flight, frees its tensor memory and returns; its output is undefined); else
- * ATTN_ERR_SEQLENS if an attn_fwd_varlen launch found invalid offsets.
+ * ATTN_ERR_SEQLENS if an attn_fwd_varlen launch found invalid offsets; else
+ * ATTN_ERR_DEBUG_CHECK if a debug-build check failed.
  * Reading clears the status. Synchronize the stream that ran the calls first.
  */
 int attn_fwd_last_error(void);

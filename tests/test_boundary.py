@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for st in range(0, -12, -1):
+    for st in range(0, -13, -1):
         s = attn.status_str(st)
         assert s and s != "unknown status", st
     assert attn.status_str(-1234) == "unknown status"
@@ -211,6 +211,23 @@ def test_ex_valid_call_without_gpu_reports_no_device(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must never reach a GPU")
 def test_valid_call_without_gpu_reports_no_device(lib):
     assert _call() == attn.ATTN_ERR_NO_DEVICE
+
+
+def test_release_build_has_no_debug_checks(lib):
+    assert lib.attn_fwd_debug_build() == 0
+    # The release build refuses the debug self-test before touching any pointer.
+    assert lib.attn_fwd_debug_selftest(A, 2 * A, 3 * A, 4 * A, 0, 1, 2, 256, 256, 128, 0.088, 0,
+                                       0) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_debug_flavour_builds_and_loads():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    build.build(debug=True)
+    dbg = attn.load_library(debug=True)
+    assert dbg.attn_fwd_debug_build() == 1
+    for name in _declared_functions():
+        assert hasattr(dbg, name), name
 
 
 def test_python_binding_checks(lib):
