@@ -391,19 +391,33 @@ def run_ours(args, w):
         dist.destroy_process_group()
         return 0
 
-    # End to end through the public API, everything inside the timed region. Fixed
-    # shapes: attn_fwd_host, the C ABI's host-buffer entry (pinned host inputs in,
-    # pinned host output back, its copies overlapped with its kernels in chunks);
-    # one call per mode, each with its own stream and workspace, each uploading
-    # its own copy of the inputs. Variable-length and split-KV workloads: the
-    # inputs go up once, then one device call per mode, each result read back.
+    # End to end through the public API, everything inside the timed region:
+    # attn_fwd_host (attn_fwd_varlen_host for a packed batch), the C ABI's
+    # host-buffer entries (pinned host inputs in, pinned host output back, the
+    # copies overlapped with the kernels in chunks); one call per mode, each with
+    # its own stream and workspace, each uploading its own copy of the inputs.
+    # Split-KV workloads: the inputs go up once, then one device call per mode,
+    # each result read back.
     qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
     host_out = {m: torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory() for m in w.roundings}
     in_bytes = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     cu_pinned = tuple(torch.from_numpy(a).pin_memory() for a in w.cu_seqlens) if w.seqlens else ()
-    host_api = not w.seqlens and splits == 1
+    host_api = splits == 1
 
-    if host_api:
+    if host_api and w.seqlens:
+        cu_host = tuple(torch.from_numpy(a) for a in w.cu_seqlens)
+        ws_bytes = attn.load_library().attn_fwd_varlen_host_workspace_bytes(
+            w.B, w.H, w.kv_heads, q_h.shape[0], k_h.shape[0], w.D)
+        e2e_ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in w.roundings]
+        e2e_streams = [torch.cuda.Stream(dev) for _ in w.roundings]
+        h2d_bytes = (in_bytes + sum(t.numel() * 4 for t in cu_host)) * len(w.roundings)
+
+        def e2e_step():
+            for i, m in enumerate(w.roundings):
+                with torch.cuda.stream(e2e_streams[i]):
+                    attn.attn_fwd_varlen_host(qp, kp, vp, *cu_host, causal=w.causal, rounding=m,
+                                              out=host_out[m], workspace=e2e_ws[i], device=dev)
+    elif host_api:
         ws_bytes = attn.host_workspace_bytes(w.B, w.H, w.kv_heads, w.Sq, w.Sk, w.D)
         e2e_ws = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in w.roundings]
         e2e_streams = [torch.cuda.Stream(dev) for _ in w.roundings]
@@ -440,7 +454,8 @@ def run_ours(args, w):
     e_ms = e0.elapsed_time(e1) / e_steps
     e2e = {"value": flops_call * len(w.roundings) / (e_ms * 1e-3) / 1e12, "unit": UNIT,
            "ms_per_step": e_ms,
-           "api": "attn_fwd_host (host buffers)" if host_api else "device buffers + copies",
+           "api": (("attn_fwd_varlen_host" if w.seqlens else "attn_fwd_host") + " (host buffers)")
+                  if host_api else "device buffers + copies",
            "h2d_bytes_per_step": h2d_bytes,
            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values())}
 

@@ -96,6 +96,12 @@ def load_library(debug: bool | None = None) -> ctypes.CDLL:
                                   + [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, i64,
                                      ctypes.c_void_p])
     lib.attn_fwd_host.restype = ctypes.c_int
+    lib.attn_fwd_varlen_host_workspace_bytes.argtypes = [i64] * 6
+    lib.attn_fwd_varlen_host_workspace_bytes.restype = i64
+    lib.attn_fwd_varlen_host.argtypes = ([ctypes.c_void_p] * 6 + [i64] * 6
+                                         + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_void_p, i64, ctypes.c_void_p])
+    lib.attn_fwd_varlen_host.restype = ctypes.c_int
     lib.attn_fwd_debug_build.argtypes = []
     lib.attn_fwd_debug_build.restype = ctypes.c_int
     lib.attn_fwd_debug_selftest.argtypes = lib.attn_fwd.argtypes
@@ -366,6 +372,59 @@ def attn_fwd_host(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     return out
 
 
+def attn_fwd_varlen_host(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool = False,
+                         scale: float | None = None, rounding: str = "rtne", out=None,
+                         workspace=None, device=None):
+    """attn_fwd_varlen on CPU tensors (pinned for overlap): q (total_q, Hq, 128),
+    k and v (total_k, Hkv, 128) bf16, cu_seqlens_q / cu_seqlens_k int32 CPU
+    tensors of B + 1 offsets. Uploads, computes and downloads in overlapped chunks
+    of whole sequences on ``device``; returns ``out`` (CPU). Asynchronous on the
+    current stream: synchronize before reading ``out``."""
+    import torch
+
+    if rounding not in ROUNDINGS:
+        raise ValueError("unknown rounding mode")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda:
+            raise TypeError(f"{name} must be a bf16 CPU tensor")
+        if t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous (tokens, heads, d) tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or t.is_cuda
+                or t.dim() != 1 or not t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous 1-D int32 CPU tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 >= 2 entries")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    if Dk != D or tuple(v.shape) != tuple(k.shape) or Hq % Hkv:
+        raise ValueError("shape mismatch")
+    if out is not None:
+        _check_out(out, q)
+    B = cu_seqlens_q.numel() - 1
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    need = load_library().attn_fwd_varlen_host_workspace_bytes(B, Hq, Hkv, total_q, total_k, D)
+    if need < 0:
+        raise AttnError(int(need), status_str(int(need)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    _check_workspace(workspace, torch.device(device))
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(device):
+        stream = torch.cuda.current_stream(device).cuda_stream
+        st = load_library().attn_fwd_varlen_host(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), cu_seqlens_q.data_ptr(),
+            cu_seqlens_k.data_ptr(), B, Hq, Hkv, total_q, total_k, D, ctypes.c_float(float(scale)),
+            ROUNDINGS[rounding], ATTN_FLAG_CAUSAL if causal else 0, workspace.data_ptr(),
+            workspace.numel(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, status_str(st))
+    return out
+
+
 def attn_fwd_last_error() -> int:
     return load_library().attn_fwd_last_error()
 
@@ -441,5 +500,5 @@ __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_
            "attn_fwd_splitkv", "attn_fwd_splitkv_raw", "splitkv_workspace_bytes",
            "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw",
            "attn_fwd_varlen", "attn_fwd_varlen_raw", "ATTN_ERR_SEQLENS",
-           "attn_fwd_host", "attn_fwd_host_raw", "host_workspace_bytes", "status_str", "load_library",
+           "attn_fwd_host", "attn_fwd_host_raw", "host_workspace_bytes", "attn_fwd_varlen_host", "status_str", "load_library",
            "AttnError", "LAYOUTS", "ROUNDINGS", "lib_path", "ATTN_ERR_DEBUG_CHECK"]

@@ -21,6 +21,10 @@
 //         A row chunk [s0, s1) of a causal problem is the causal problem with
 //         Sq' = s1 - s0 and Sk' = s1 + Sk - Sq: row i' sees keys up to
 //         i' + s0 + Sk - Sq, the same keys as row s0 + i' of the whole problem.
+//   packed variable-length batch (attn_fwd_varlen_host): runs of whole
+//         sequences, contiguous in the packed tensors; a chunk's kernel is
+//         attn_fwd_varlen over the full tensors with the offsets array advanced
+//         to its first sequence (the offsets stay absolute).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -133,6 +137,33 @@ std::vector<Chunk> plan(int layout, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
   return out;
 }
 
+// Runs of whole sequences of a packed batch, at most kMaxChunks, each of at
+// least kCtasPerChunk CTAs where the batch allows.
+struct SeqChunk {
+  int64_t b0, b1, max_sq;
+};
+
+std::vector<SeqChunk> plan_varlen(const int32_t* cq, int64_t B, int64_t Hq) {
+  int64_t total = 0;
+  for (int64_t b = 0; b < B; ++b) total += Hq * qpairs(cq[b + 1] - cq[b]);
+  int64_t want = total / kCtasPerChunk;
+  want = want < 1 ? 1 : (want > kMaxChunks ? kMaxChunks : want);
+  std::vector<SeqChunk> out;
+  int64_t b0 = 0, acc = 0, max_sq = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t sq = cq[b + 1] - cq[b];
+    acc += Hq * qpairs(sq);
+    max_sq = sq > max_sq ? sq : max_sq;
+    const int64_t goal = total * (static_cast<int64_t>(out.size()) + 1) / want;
+    if (acc >= goal || b == B - 1) {
+      out.push_back({b0, b + 1, max_sq});
+      b0 = b + 1;
+      max_sq = 0;
+    }
+  }
+  return out;
+}
+
 }  // namespace
 
 extern "C" {
@@ -219,6 +250,118 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* out, int la
     if (!ok) status = ATTN_ERR_LAUNCH;
   }
   // The caller's stream waits for everything enqueued above, also after an error.
+  ok = cudaEventRecord(ds.comp_done[0], ds.comp[0]) == cudaSuccess &&
+       cudaEventRecord(ds.comp_done[1], ds.comp[1]) == cudaSuccess &&
+       cudaEventRecord(ds.done, ds.out) == cudaSuccess &&
+       cudaStreamWaitEvent(caller, ds.comp_done[0], 0) == cudaSuccess &&
+       cudaStreamWaitEvent(caller, ds.comp_done[1], 0) == cudaSuccess &&
+       cudaStreamWaitEvent(caller, ds.done, 0) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    if (status == ATTN_OK) status = ATTN_ERR_LAUNCH;
+  }
+  return status;
+}
+
+int64_t attn_fwd_varlen_host_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t total_q,
+                                             int64_t total_k, int64_t d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || total_q < 1 || total_k < 1 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  const int64_t kLim = (int64_t(1) << 31) - 1;
+  if (B > kLim || total_q > kLim || total_k > kLim || Hq > kLim) return ATTN_ERR_TOO_LARGE;
+  return 2 * round_up(total_q * Hq * 256, kAlign) + 2 * round_up(total_k * Hkv * 256, kAlign) +
+         2 * round_up((B + 1) * 4, kAlign);
+}
+
+int attn_fwd_varlen_host(const void* q, const void* k, const void* v, void* out,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t B,
+                         int64_t Hq, int64_t Hkv, int64_t total_q, int64_t total_k, int64_t d,
+                         float scale, int rounding_mode, int flags, void* workspace,
+                         int64_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  const int64_t need = attn_fwd_varlen_host_workspace_bytes(B, Hq, Hkv, total_q, total_k, d);
+  if (need < 0) return static_cast<int>(need);
+  if (!(scale - scale == 0.f)) return ATTN_ERR_INVALID_ARG;  // NaN or Inf
+  if (flags & ~ATTN_FLAG_CAUSAL) return ATTN_ERR_UNSUPPORTED;
+  if (rounding_mode < ATTN_ROUND_RTNE || rounding_mode > ATTN_ROUND_RTZ) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) return ATTN_ERR_MISALIGNED;
+  // The offsets are on the host here, so they are checked before anything runs.
+  if (cu_seqlens_q[0] != 0 || cu_seqlens_k[0] != 0 || cu_seqlens_q[B] != total_q ||
+      cu_seqlens_k[B] != total_k)
+    return ATTN_ERR_SEQLENS;
+  for (int64_t b = 0; b < B; ++b)
+    if (cu_seqlens_q[b + 1] < cu_seqlens_q[b] || cu_seqlens_k[b + 1] < cu_seqlens_k[b])
+      return ATTN_ERR_SEQLENS;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  DeviceStreams& ds = g_dev[dev];
+  std::lock_guard<std::mutex> lock(ds.mu);
+  const int st0 = setup(ds);
+  if (st0 != ATTN_OK) return st0;
+
+  const std::vector<SeqChunk> chunks = plan_varlen(cu_seqlens_q, B, Hq);
+  const int64_t q_region = round_up(total_q * Hq * 256, kAlign);
+  const int64_t kv_region = round_up(total_k * Hkv * 256, kAlign);
+  const int64_t cu_region = round_up((B + 1) * 4, kAlign);
+  char* wq = static_cast<char*>(workspace);
+  char* wo = wq + q_region;
+  char* wk = wo + q_region;
+  char* wv = wk + kv_region;
+  int32_t* wcq = reinterpret_cast<int32_t*>(wv + kv_region);
+  int32_t* wck = reinterpret_cast<int32_t*>(wv + kv_region + cu_region);
+  const char* hq = static_cast<const char*>(q);
+  const char* hk = static_cast<const char*>(k);
+  const char* hv = static_cast<const char*>(v);
+  char* ho = static_cast<char*>(out);
+  const int64_t qrow = Hq * 256, kvrow = Hkv * 256;  // bytes per token
+  const cudaStream_t caller = static_cast<cudaStream_t>(stream);
+
+  bool ok = cudaEventRecord(ds.start, caller) == cudaSuccess;
+  for (cudaStream_t s : {ds.in, ds.out, ds.comp[0], ds.comp[1]})
+    ok = ok && cudaStreamWaitEvent(s, ds.start, 0) == cudaSuccess;
+  // The offsets go up first (they are small); every chunk's kernel reads them.
+  ok = ok && cudaMemcpyAsync(wcq, cu_seqlens_q, (B + 1) * 4, cudaMemcpyHostToDevice, ds.in) ==
+                 cudaSuccess &&
+       cudaMemcpyAsync(wck, cu_seqlens_k, (B + 1) * 4, cudaMemcpyHostToDevice, ds.in) ==
+           cudaSuccess;
+  int status = ok ? ATTN_OK : ATTN_ERR_LAUNCH;
+  for (size_t i = 0; i < chunks.size() && status == ATTN_OK; ++i) {
+    const SeqChunk& c = chunks[i];
+    const cudaStream_t cs = ds.comp[i & 1];
+    const int64_t q0 = cu_seqlens_q[c.b0], q1 = cu_seqlens_q[c.b1];
+    const int64_t k0 = cu_seqlens_k[c.b0], k1 = cu_seqlens_k[c.b1];
+    ok = true;
+    if (q1 > q0)
+      ok = cudaMemcpyAsync(wq + q0 * qrow, hq + q0 * qrow, (q1 - q0) * qrow,
+                           cudaMemcpyHostToDevice, ds.in) == cudaSuccess;
+    if (ok && k1 > k0)
+      ok = cudaMemcpyAsync(wk + k0 * kvrow, hk + k0 * kvrow, (k1 - k0) * kvrow,
+                           cudaMemcpyHostToDevice, ds.in) == cudaSuccess &&
+           cudaMemcpyAsync(wv + k0 * kvrow, hv + k0 * kvrow, (k1 - k0) * kvrow,
+                           cudaMemcpyHostToDevice, ds.in) == cudaSuccess;
+    ok = ok && cudaEventRecord(ds.landed[i], ds.in) == cudaSuccess &&
+         cudaStreamWaitEvent(cs, ds.landed[i], 0) == cudaSuccess;
+    if (!ok) {
+      status = ATTN_ERR_LAUNCH;
+      break;
+    }
+    if (c.max_sq == 0) continue;  // only sequences without queries
+    status = attn_fwd_varlen(wq, wk, wv, wo, wcq + c.b0, wck + c.b0, c.b1 - c.b0, Hq, Hkv,
+                             total_q, total_k, c.max_sq, d, scale, rounding_mode, flags, cs);
+    if (status != ATTN_OK) break;
+    ok = cudaEventRecord(ds.computed[i], cs) == cudaSuccess &&
+         cudaStreamWaitEvent(ds.out, ds.computed[i], 0) == cudaSuccess &&
+         cudaMemcpyAsync(ho + q0 * qrow, wo + q0 * qrow, (q1 - q0) * qrow, cudaMemcpyDeviceToHost,
+                         ds.out) == cudaSuccess;
+    if (!ok) status = ATTN_ERR_LAUNCH;
+  }
   ok = cudaEventRecord(ds.comp_done[0], ds.comp[0]) == cudaSuccess &&
        cudaEventRecord(ds.comp_done[1], ds.comp[1]) == cudaSuccess &&
        cudaEventRecord(ds.done, ds.out) == cudaSuccess &&

@@ -241,6 +241,28 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* out, int la
                   void* stream);
 
 /*
+ * attn_fwd_varlen_host - attn_fwd_varlen on HOST buffers, copies overlapped.
+ *   q, k, v, out       host memory, packed (token, head, d) as attn_fwd_varlen
+ *   cu_seqlens_q/_k    HOST int32 arrays of B + 1 offsets; being on the host they
+ *                      are checked before anything runs (ATTN_ERR_SEQLENS: not
+ *                      starting at 0, decreasing, or not ending at the totals)
+ *   workspace          device memory of attn_fwd_varlen_host_workspace_bytes()
+ *                      bytes, 256-byte aligned (copies of the four tensors and
+ *                      of both offset arrays)
+ * Chunks are runs of whole sequences (contiguous in every tensor); each chunk's
+ * upload, attn_fwd_varlen launch and download run on internal streams ordered
+ * by events, as attn_fwd_host. Stream, ownership and results as attn_fwd_host
+ * (bit-identical to attn_fwd_varlen). No counterpart on the pages.
+ */
+int64_t attn_fwd_varlen_host_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t total_q,
+                                             int64_t total_k, int64_t d);
+int attn_fwd_varlen_host(const void* q, const void* k, const void* v, void* out,
+                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t B,
+                         int64_t Hq, int64_t Hkv, int64_t total_q, int64_t total_k, int64_t d,
+                         float scale, int rounding_mode, int flags, void* workspace,
+                         int64_t workspace_bytes, void* stream);
+
+/*
  * Debug build. The library built with -DATTN_DEBUG=1 (libattn_fwd_debug.so)
  * checks, inside the kernel, every computed tile coordinate, global row index
  * and the producer's count of ring fills; a failed check skips the access it

@@ -174,6 +174,13 @@ def _host(q=A, k=2 * A, v=3 * A, o=4 * A, layout=1, B=2, Hq=16, Hkv=16, Sq=8192,
                                   max(need, 0), 0)
 
 
+def test_varlen_host_workspace_bytes(lib):
+    n = lib.attn_fwd_varlen_host_workspace_bytes(3, 8, 2, 1000, 1500, 128)
+    assert n == 2 * 1000 * 8 * 256 + 2 * 1500 * 2 * 256 + 2 * 256
+    assert lib.attn_fwd_varlen_host_workspace_bytes(3, 8, 3, 1000, 1500, 128) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_varlen_host_workspace_bytes(3, 8, 2, 0, 1500, 128) == attn.ATTN_ERR_INVALID_ARG
+
+
 def test_host_buffer_workspace_bytes(lib):
     assert attn.host_workspace_bytes(2, 16, 4, 8192, 1000) == 2 * 2 * 16 * 8192 * 256 + 2 * 2 * 4 * 1000 * 256
     assert attn.host_workspace_bytes(1, 1, 1, 1, 1) == 4 * 256

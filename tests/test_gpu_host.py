@@ -73,3 +73,31 @@ def test_host_calls_on_two_streams_with_two_workspaces():
     want_b = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), layout="bshd", rounding="rtz").cpu()
     assert torch.equal(a.view(torch.int16), want_a.view(torch.int16))
     assert torch.equal(b.view(torch.int16), want_b.view(torch.int16))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_host_equals_device_call_bitwise(causal):
+    # Enough sequences and rows for several chunks of whole sequences, with a
+    # sequence without queries and one without keys among them.
+    lens = ((700, 900), (0, 5), (2048, 2048), (300, 0), (4096, 3000), (129, 129), (1500, 1600),
+            (4000, 4100))
+    w = inputs.Workload("vh", "thd", len(lens), 16, 4096, 4100, seed=1310, hkv=4, seqlens=lens)
+    q, k, v = inputs.make_qkv(w)
+    cq, ck = w.cu_seqlens
+    got = attn.attn_fwd_varlen_host(q.pin_memory(), k.pin_memory(), v.pin_memory(),
+                                    torch.from_numpy(cq), torch.from_numpy(ck), causal=causal)
+    want = attn.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cq).cuda(),
+                                torch.from_numpy(ck).cuda(), 4096, causal=causal)
+    torch.cuda.synchronize()
+    assert attn.attn_fwd_last_error() == attn.ATTN_OK
+    assert torch.equal(got.view(torch.int16), want.cpu().view(torch.int16))
+
+
+def test_varlen_host_rejects_bad_offsets_before_running():
+    w = inputs.Workload("vh", "thd", 2, 2, 100, 100, seed=1311, seqlens=((100, 100), (100, 100)))
+    q, k, v = inputs.make_qkv(w)
+    for cq in ([0, 210, 200], [0, 100, 150], [1, 100, 200]):  # decreasing, short, not from 0
+        with pytest.raises(attn.AttnError) as e:
+            attn.attn_fwd_varlen_host(q, k, v, torch.tensor(cq, dtype=torch.int32),
+                                      torch.tensor([0, 100, 200], dtype=torch.int32))
+        assert e.value.status in (attn.ATTN_ERR_SEQLENS, attn.ATTN_ERR_INVALID_ARG)
