@@ -53,7 +53,8 @@ def _peaks():
 
 KERNEL_SOURCES = ("bf16_forward_attention_gb300/csrc/attn_fwd_kernel.cuh",
                   "bf16_forward_attention_gb300/csrc/ptx.cuh",
-                  "bf16_forward_attention_gb300/csrc/attn_fwd.cu")
+                  "bf16_forward_attention_gb300/csrc/attn_fwd.cu",
+                  "bf16_forward_attention_gb300/csrc/splitkv_combine.cuh")
 
 
 def kernel_sources_hash() -> str:

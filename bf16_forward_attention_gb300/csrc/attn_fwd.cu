@@ -271,7 +271,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
     cp.sq_pad = p.sq_pad;
     cp.layout = layout;
     cp.mode = rounding_mode;
-    attn::attn_splitkv_combine<<<dim3(static_cast<unsigned>(Sq), static_cast<unsigned>(B * H)),
+    attn::attn_splitkv_combine<<<dim3(static_cast<unsigned>((Sq + attn::kCombineRows - 1) /
+                                                            attn::kCombineRows),
+                                      static_cast<unsigned>(B * H)),
                                  attn::kD, 0, cs>>>(cp);
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
