@@ -37,6 +37,21 @@ os.environ.setdefault("OMP_NUM_THREADS", str(_CPU_THREADS))
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
+
+def _blas_threads() -> int:
+    """Threads the oracle's BLAS runs with: as the BLAS reports it where
+    threadpoolctl is installed, else the environment setting above (which a
+    caller may have preset)."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001 - optional dependency
+        pass
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", _CPU_THREADS))
+
 METRIC = "attention fwd TFLOP/s (4·B·H·Sq·Sk·d) and % of GB300 dense bf16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
@@ -293,7 +308,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / max(1, len(done)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(w, world),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                          "sample": f"{rows} query rows of the workload, each against {_keys_seen(w)} "
                                    f"(~{step_s:.2g} s of fp64 CPU work per step)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -471,7 +486,7 @@ def run_ours(args, w):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         f, t, rows = _cpu_sample(w, q_h, k_h, v_h, budget_s=args.cpu_seconds)
-        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": _CPU_THREADS, "kind": "oracle",
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{rows} query rows of the workload, each against {_keys_seen(w)} "
                          f"({t:.1f} s of fp64 CPU work)"}
 
