@@ -29,7 +29,8 @@ Readings where the pages are silent (each is listed in the design notes):
   * every NaN output is written as the one pattern 0x7FC0.
   * causal (a follow-on step the pages name as missing): key j is visible to
     query i iff j <= i + (Sk - Sq), the bottom-right alignment that makes the last
-    query see every key; hidden logits are -Inf, so a row that sees no key is NaN.
+    query see every key; hidden keys take no part (logit -Inf, and left out of the
+    product with V), so a row that sees no key is NaN.
   * grouped-query attention (also named as missing): Hq query heads share Hkv
     key/value heads, query head h reads K/V head h // (Hq // Hkv).
   * variable-length batches (also named as missing, as cu_seqlens batching):
@@ -86,7 +87,10 @@ def attention_rows_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: floa
       l_i  = sum_j p_ij
       O_ic = (sum_j p_ij v_jc) / l_i
     The matrix products are library primitives; nothing is blocked or fused across
-    the key axis. With causal, s_ij = -Inf for j > i + (Sk - Sq).
+    the key axis. With causal, key j is hidden from row i when j > i + (Sk - Sq):
+    s_ij = -Inf (so p_ij = 0), and the hidden keys take no part in the product
+    either, so a non-finite value of V at a key a row does not see cannot reach
+    that row (0 * NaN would).
     """
     scale_d = float(np.float32(scale))
     Sq_all, Sk = q.shape[0], k.shape[0]
@@ -94,13 +98,21 @@ def attention_rows_fp64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: floa
     q = q[idx]
     s = _ieee_matmul(q, k.T) * scale_d
     if causal:
-        hidden = np.arange(Sk)[None, :] > (idx[:, None] + (Sk - Sq_all))
-        s = np.where(hidden, -np.inf, s)
+        visible = np.clip(idx + (Sk - Sq_all) + 1, 0, Sk)  # keys 0 .. visible-1
+        s = np.where(np.arange(Sk)[None, :] >= visible[:, None], -np.inf, s)
     with np.errstate(invalid="ignore", over="ignore"):
         m = np.max(s, axis=1, keepdims=True)  # np.max propagates NaN
         p = np.exp(s - m)
         l = np.sum(p, axis=1, keepdims=True)
-        o = _ieee_matmul(p, v) / l
+        if causal and not np.isfinite(v).all():
+            # Row by row over the visible keys only (a row that sees none is NaN).
+            num = np.full((idx.size, v.shape[1]), np.nan)
+            for r in range(idx.size):
+                if visible[r] > 0:
+                    num[r] = _ieee_matmul(p[r:r + 1, :visible[r]], v[:visible[r]])[0]
+            o = num / l
+        else:
+            o = _ieee_matmul(p, v) / l
     return o
 
 

@@ -15,7 +15,7 @@ import torch
 
 import bf16_forward_attention_gb300 as attn
 from bf16_forward_attention_gb300 import build, inputs
-from oracle import attention_fp64, attention_rows_fp64, to_bhsd
+from oracle import attention_fp64, attention_rows_fp64, nonfinite_bits, round_bf16, to_bhsd
 
 from _parity import assert_parity, bits_of, compare, f64_of
 
@@ -202,3 +202,52 @@ def test_full_size_sampled(name):
         again = attn.attn_fwd(qd, kd, vd, layout=w.layout, rounding=w.roundings[-1])
         torch.cuda.synchronize()
         assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+
+
+def _v_specials(layout, causal, plant):
+    w = inputs.Workload("vs", layout, 1, 2, 300, 300, seed=90)
+    q, k, v = inputs.make_qkv(w)
+    vb = v.view(torch.int16).numpy()  # bf16 bit patterns, in place
+    for (h, j, c, bits) in plant:
+        vb[index_of_layout(layout, 0, h, j, c)] = np.uint16(bits).view(np.int16)
+    out = attn.attn_fwd_ex(q.cuda(), k.cuda(), v.cuda(), causal=causal, layout=layout)
+    torch.cuda.synchronize()
+    exact = attention_fp64(f64_of(q), f64_of(k), f64_of(v), inputs.default_scale(), layout,
+                           causal=causal)
+    return bits_of(out), exact
+
+
+def index_of_layout(layout, b, h, s, c):
+    return (b, h, s, c) if layout == "bhsd" else (b, s, h, c)
+
+
+@pytest.mark.parametrize("layout", ["bhsd", "bshd"])
+def test_nan_in_v_propagates_exactly(layout):
+    got, exact = _v_specials(layout, False, [(0, 17, 5, 0x7FC0), (1, 299, 100, 0xFFC1)])
+    stats = compare(got, exact, "rtne")
+    assert stats["n_nonfinite"] == 2 * 300
+    assert_parity(stats)
+
+
+def test_nan_in_v_at_a_key_every_causal_row_sees():
+    got, exact = _v_specials("bhsd", True, [(0, 0, 3, 0x7FC0)])
+    stats = compare(got, exact, "rtne")
+    assert stats["n_nonfinite"] == 300
+    assert_parity(stats, excess=True)
+
+
+def test_inf_in_v_positions():
+    # +-Inf in V: the exact output is +-Inf in that column (p > 0 times Inf). The
+    # kernel's two-term P meets it as P_hi*Inf + P_lo*Inf, where P_lo <= 0 or 0
+    # gives Inf - Inf or 0 * Inf = NaN: the positions are exact, the pattern may be
+    # the NaN instead of the Inf (a documented deviation).
+    got, exact = _v_specials("bshd", False, [(0, 40, 8, 0x7F80), (1, 200, 77, 0xFF80)])
+    want = round_bf16(exact, "rtne")
+    nf_w, nf_g = nonfinite_bits(want), nonfinite_bits(got)
+    assert nf_w.sum() == 2 * 300 and (nf_w == nf_g).all()
+    ok = (got[nf_w] == want[nf_w]) | (got[nf_w] == 0x7FC0)
+    assert ok.all()
+    finite = ~nf_w
+    fin_stats = compare(np.where(finite, got, 0).astype(np.uint16), np.where(finite, exact, 0.0),
+                        "rtne")
+    assert_parity(fin_stats)

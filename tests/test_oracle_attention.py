@@ -373,3 +373,21 @@ def test_varlen_empty_sequences():
     np.testing.assert_allclose(got[4:7], want[0].swapaxes(0, 1), rtol=1e-12, atol=1e-13)
     with pytest.raises(ValueError):
         oracle.attention_varlen_fp64(q, k, v, [0, 4, 3, 7], ck, 0.1)
+
+
+def test_causal_hidden_keys_take_no_part_even_with_nonfinite_v():
+    q, k, v = _rand((1, 1, 6, 128), 80), _rand((1, 1, 6, 128), 81), _rand((1, 1, 6, 128), 82)
+    v_bad = v.copy()
+    v_bad[0, 0, 4, 7] = np.nan      # key 4: seen by rows 4 and 5 only
+    v_bad[0, 0, 5, 9] = np.inf      # key 5: seen by row 5 only
+    got = attention_fp64(q, k, v_bad, 0.1, causal=True)
+    clean = attention_fp64(q, k, v, 0.1, causal=True)
+    # Rows 0..3 see neither key: the clean result (up to summation order).
+    np.testing.assert_allclose(got[0, 0, :4], clean[0, 0, :4], rtol=1e-13, atol=1e-15)
+    # Row i equals the unmasked definition over keys 0..i (the row's own truncated
+    # problem); non-finite positions exactly.
+    for i in range(6):
+        want = attention_rows_fp64(q[0, 0], k[0, 0, :i + 1], v_bad[0, 0, :i + 1], 0.1, [i])[0]
+        np.testing.assert_allclose(got[0, 0, i], want, rtol=1e-13, atol=1e-15)
+    assert np.isnan(got[0, 0, 4:, 7]).all()
+    assert got[0, 0, 5, 9] == np.inf and np.isfinite(got[0, 0, 4, 9])
