@@ -170,6 +170,16 @@ class Workload:
         ck = np.concatenate([[0], np.cumsum([b for _, b in self.seqlens])]).astype(np.int32)
         return cq, ck
 
+    @property
+    def io_bytes(self) -> int:
+        """Algorithmic bytes of one call: Q, K, V read once and O written once, bf16
+        (K and V once per key/value head: the query tiles of a head share them)."""
+        if self.seqlens:
+            tq = sum(a for a, _ in self.seqlens)
+            tk = sum(b for _, b in self.seqlens)
+            return 2 * self.D * (2 * tq * self.H + 2 * tk * self.kv_heads)
+        return 2 * self.D * self.B * (2 * self.Sq * self.H + 2 * self.Sk * self.kv_heads)
+
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
@@ -203,6 +213,11 @@ WORKLOADS = {
                          seed=20260007, causal=True),
     "gqa8k": Workload("gqa8k", "bshd", 2, 16, 8192, 8192, roundings=("rtne",),
                       seed=20260008, hkv=4),
+    # Short key range: 16K query tokens against a 77-token context (the shape of
+    # text cross-attention in image and video diffusion). Q and O dominate the
+    # bytes, so the call is bound by HBM bandwidth, not by the tensor pipe.
+    "short77": Workload("short77", "bshd", 2, 32, 16384, 77, roundings=("rtne",),
+                        seed=20260010),
 }
 # Variable-length self-attention batch: 16 sequences of seeded lengths 256..16384
 # (a mix around the 8K case), 16 heads, packed token after token.

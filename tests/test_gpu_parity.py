@@ -159,7 +159,7 @@ def _closed_form_nonfinite_rows(w, q):
     return mask
 
 
-@pytest.mark.parametrize("name", ["self8k", "cross4k32k", "long128k", "stress16381"])
+@pytest.mark.parametrize("name", ["self8k", "cross4k32k", "long128k", "stress16381", "short77"])
 def test_full_size_sampled(name):
     w = inputs.WORKLOADS[name]
     q, k, v = inputs.make_qkv(w)
