@@ -40,6 +40,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 = not set up, 1 = ready, negative = status to return
+int g_dev_sms[kMaxDevices];    // streaming multiprocessors of each device (once ready)
+
+// Whole-range problems with at most this many key tiles run on the persistent
+// variant (one CTA per SM looping over the items) when they have more items
+// than SMs: their items are short, and one CTA per item leaves each SM idle
+// through every item's first loads and final store.
+constexpr int64_t kPersistMaxKvTiles = 16;
 
 // Once per device: check the architecture and raise the shared-memory limit.
 int device_ready(int dev) {
@@ -63,10 +70,12 @@ int device_ready(int dev) {
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true>),
-      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>)};
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>)};
   for (const void* fn : variants) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, attn::kSmemBytes) !=
-        cudaSuccess) {
+    const bool persist = fn == variants[5];
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             persist ? attn::kSmemBytesPersist : attn::kSmemBytes) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
@@ -86,6 +95,12 @@ int device_ready(int dev) {
       return ATTN_ERR_LAUNCH;
     }
   }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  g_dev_sms[dev] = sms;
   g_dev_state[dev] = 1;
   return ATTN_OK;
 }
@@ -248,12 +263,17 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.out = static_cast<uint16_t*>(out);
   p.head_group = head_group_of(B * H, Sk);
   p.dbg_poison = dbg_poison;
+  p.n_items = static_cast<int>(B * H * n_qpairs * n_splits);
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
   if (causal) {
     attn::attn_fwd_kernel<false, true, false>
         <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+  } else if (n_splits == 1 && p.kv_tiles <= kPersistMaxKvTiles && p.n_items > g_dev_sms[dev]) {
+    attn::attn_fwd_kernel<false, false, false, true>
+        <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
+            tq, tk, tv, to, p);
   } else if (n_splits == 1) {
     attn::attn_fwd_kernel<false, false, false>
         <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
@@ -375,6 +395,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
   p.out = static_cast<uint16_t*>(out);
   p.head_group = p.causal ? head_group_of(B * Hq, total_k / B) : 1;
   p.dbg_poison = 0;
+  p.n_items = static_cast<int>(B * Hq * n_qpairs);
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * Hq * n_qpairs);

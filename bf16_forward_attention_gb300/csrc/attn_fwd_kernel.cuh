@@ -81,7 +81,9 @@ enum : int {
   kBarPFull = kBarSFull + kQTiles,
   kBarOFull = kBarPFull + kQTiles,
   kBarDrain = kBarOFull + kQTiles,
-  kBarCount = kBarDrain + 1
+  kBarQFree = kBarDrain + 1,  // persistent: the Q buffer may be refilled (next item)
+  kBarOFree = kBarQFree + 1,  // persistent, per query tile: the epilogue has read O
+  kBarCount = kBarOFree + kQTiles
 };
 
 constexpr int kOffQ = 0;
@@ -92,6 +94,13 @@ constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// The persistent variant also stages its output: 4 KiB per softmax warp (32
+// rows x 64 columns, one TMA box), so that the Q buffer can be refilled for the
+// next item while the current one is being stored.
+constexpr int kStageWarpBytes = 32 * 128;
+constexpr int kOffStage = (kSmemUsed + 1023) & ~1023;
+constexpr int kSmemBytesPersist = kOffStage + 8 * kStageWarpBytes + 1024;
+static_assert(kSmemBytesPersist <= 232448, "shared memory budget (persistent)");
 
 constexpr uint32_t kTmemO0 = 0, kTmemS0 = 256;
 
@@ -120,6 +129,7 @@ struct Params {
   uint16_t* out;    // output base, for rows stored without TMA
   int head_group;   // causal: (batch, head) items scheduled together, longest first
   int dbg_poison;   // debug build only: report one failed check (tests the reporting)
+  int n_items;      // persistent variant: work items; CTA c takes c, c + gridDim.x, ...
 };
 
 // Bit 0: some wait timed out. Bit 1: a variable-length batch's offsets were
@@ -246,6 +256,15 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
     u += 0x8000u;  // nearest, ties away from zero (sign-magnitude)
   }                // mode 2: toward zero = truncate
   return u >> 16;
+}
+
+// round_bf16_bits with the mode's constants hoisted out of the element loop: one
+// add before the truncation, bias 0x7FFF plus the kept lowest bit (lsb_mask 1)
+// for RTNE, 0x8000 for RTNA, 0 for RTZ; NaN gives the one pattern 0x7FC0.
+__device__ __forceinline__ uint32_t round_bf16_biased(float x, uint32_t bias, uint32_t lsb_mask) {
+  const uint32_t u = __float_as_uint(x);
+  const uint32_t r = (u + bias + ((u >> 16) & lsb_mask)) >> 16;
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC0u : r;
 }
 
 // The running output row of a softmax thread: 128 fp32 as 64 packed pairs
@@ -451,10 +470,10 @@ struct Work {
 };
 
 template <bool kCausal, bool kVarlen>
-__device__ __forceinline__ Work work_of(const Params& p) {
+__device__ __forceinline__ Work work_of(const Params& p, int work_item) {
   Work w;
-  w.split = blockIdx.x % p.n_splits;
-  const int item = blockIdx.x / p.n_splits;
+  w.split = work_item % p.n_splits;
+  const int item = work_item / p.n_splits;
   if (kCausal || kVarlen) {
     // Causal pairs differ in length: within each group of head_group (batch,
     // head) items, longest key ranges first (blocks start in index order, so
@@ -508,13 +527,25 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   return w;
 }
 
+// The CTA's own work item (one item per CTA).
+template <bool kCausal, bool kVarlen>
+__device__ __forceinline__ Work work_of(const Params& p) {
+  return work_of<kCausal, kVarlen>(p, blockIdx.x);
+}
+
 // kPartial: the CTA covers one split of the key range and writes its fp32 partial
 // result to the workspace (combined by attn_splitkv_combine); otherwise the CTA
 // covers all keys and stores bf16 output. kCausal: the causal mask (p.causal
 // must agree). kVarlen: a packed batch of variable-length sequences, one grid
-// slot per (sequence, head, query-tile pair) up to the longest sequence. Each is
-// compiled separately so that the other variants carry none of it.
-template <bool kPartial, bool kCausal, bool kVarlen>
+// slot per (sequence, head, query-tile pair) up to the longest sequence.
+// kPersist (whole key range, no mask only): each CTA loops over items c,
+// c + gridDim.x, ... with the barrier phases carried from item to item, the next
+// item's Q loaded as soon as the current item's last S MMAs are done, and the
+// output stored through a staging area of its own; used for short key ranges,
+// where an item's fixed latency (first loads, epilogue, store) would otherwise
+// leave the SM idle. Each is compiled separately so that the other variants
+// carry none of it.
+template <bool kPartial, bool kCausal, bool kVarlen, bool kPersist = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -529,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sRing = sbase + kOffRing;
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
 
+  static_assert(!kPersist || (!kPartial && !kCausal && !kVarlen), "persistent: base path only");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // A key limit per row (rising along the causal diagonal, or the sequence's
@@ -568,6 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(kBarOFull + t), 1);
     }
     ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::mbar_init(bar(kBarQFree), 1);
+    for (int t = 0; t < kQTiles; ++t) ptx::mbar_init(bar(kBarOFree + t), 128);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -593,97 +627,222 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::setmaxnreg_dec<kRegsLow>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
-      if (lane == 0) {
-        const Work wk = work_of<kCausal, kVarlen>(p);
-        const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
-        const int kv_head = wk.kv_head, q_base = wk.q_base, k_base = wk.k_base;
-        int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
-        int c1, c2;
-        dbg_ok(q_base + 2 * pair * kBM < p.Sq);  // the first query tile starts inside
-        ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
-        for (int t = 0; t < kQTiles; ++t) {
-          tma_coords(p.layout, q_base + (2 * pair + t) * kBM, head, c1, c2);
-          for (int hf = 0; hf < 2; ++hf)
-            ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
-                             batch);
+      if constexpr (kPersist) {
+        if (lane == 0) {
+          int issued = 0;   // ring fills started so far (fill i goes to stage i % kStages)
+          int planned = 0;  // ring fills of the items started so far
+          int q_loads = 0;  // Q loads started so far (load i completes phase i of kBarQ)
+          int c1, c2;
+          for (int item = blockIdx.x, iter = 0; item < p.n_items; item += gridDim.x, ++iter) {
+            const Work wk = work_of<kCausal, kVarlen>(p, item);
+            // The Q buffer is free once the previous item's last S MMAs are done.
+            if (iter > 0 && !wait_bounded(bar(kBarQFree), (iter - 1) & 1, abort_flag, p.timeout_ns, true))
+              break;
+            dbg_ok(wk.q_base + 2 * wk.pair * kBM < p.Sq);  // the first query tile starts inside
+            ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
+            for (int t = 0; t < kQTiles; ++t) {
+              tma_coords(p.layout, wk.q_base + (2 * wk.pair + t) * kBM, wk.head, c1, c2);
+              for (int hf = 0; hf < 2; ++hf)
+                ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1,
+                                 c2, wk.batch);
+            }
+            ++q_loads;
+            planned += 2 * wk.n_kv;
+            bool ok = true;
+            for (int it = 0; it < 2 * wk.n_kv; ++it) {
+              const int stage = issued % kStages;
+              const uint32_t parity = ((issued / kStages) & 1) ^ 1;
+              if (!(ok = wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)))
+                break;
+              const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+              dbg_ok(wk.k_base + (wk.tile0 + (it >> 1)) * kBN < p.Sk + kBN);
+              tma_coords(p.layout, wk.k_base + (wk.tile0 + (it >> 1)) * kBN, wk.kv_head, c1, c2);
+              ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
+              for (int hf = 0; hf < 2; ++hf)
+                ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map,
+                                 bar(kBarKvFull + stage), 64 * hf, c1, c2, wk.batch);
+              ++issued;
+            }
+            if (!ok) break;
+          }
+          // Let every copy this thread started land before the CTA can exit. On
+          // the normal path these phases have long completed; after an abort the
+          // consumer may never have waited for them. (At most one Q load is ever
+          // outstanding: the next waits for the S MMAs that consume it.)
+          dbg_ok(issued == planned || *abort_flag);  // every fill of the plan was issued
+          if (q_loads > 0) wait_bounded(bar(kBarQ), (q_loads - 1) & 1, abort_flag, p.timeout_ns, false);
+          for (int s = 0; s < kStages && s < issued; ++s) {
+            const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
+            wait_bounded(bar(kBarKvFull + s), (fills - 1) & 1, abort_flag, p.timeout_ns, false);
+          }
         }
-        for (int it = 0; it < 2 * n_kv; ++it) {
-          const int stage = it % kStages;
-          const uint32_t parity = ((it / kStages) & 1) ^ 1;
-          if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
-          const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-          dbg_ok(k_base + (tile0 + (it >> 1)) * kBN < p.Sk + kBN);
-          tma_coords(p.layout, k_base + (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
-          ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
-          for (int hf = 0; hf < 2; ++hf)
-            ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
-                             64 * hf, c1, c2, batch);
-          ++issued;
-        }
-        // Let every copy this thread started land before the CTA can exit. On
-        // the normal path these phases have long completed; after an abort the
-        // consumer may never have waited for them.
-        dbg_ok(issued == 2 * n_kv || *abort_flag);  // every fill of the plan was issued
-        wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
-        for (int s = 0; s < kStages && s < issued; ++s) {
-          const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
-          wait_bounded(bar(kBarKvFull + s), (fills - 1) & 1, abort_flag, p.timeout_ns, false);
+      } else {
+        if (lane == 0) {
+          const Work wk = work_of<kCausal, kVarlen>(p);
+          const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
+          const int kv_head = wk.kv_head, q_base = wk.q_base, k_base = wk.k_base;
+          int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
+          int c1, c2;
+          dbg_ok(q_base + 2 * pair * kBM < p.Sq);  // the first query tile starts inside
+          ptx::mbar_arrive_expect_tx(bar(kBarQ), kQTiles * kTileBytes);
+          for (int t = 0; t < kQTiles; ++t) {
+            tma_coords(p.layout, q_base + (2 * pair + t) * kBM, head, c1, c2);
+            for (int hf = 0; hf < 2; ++hf)
+              ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
+                               batch);
+          }
+          for (int it = 0; it < 2 * n_kv; ++it) {
+            const int stage = it % kStages;
+            const uint32_t parity = ((it / kStages) & 1) ^ 1;
+            if (!wait_bounded(bar(kBarKvEmpty + stage), parity, abort_flag, p.timeout_ns, true)) break;
+            const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+            dbg_ok(k_base + (tile0 + (it >> 1)) * kBN < p.Sk + kBN);
+            tma_coords(p.layout, k_base + (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
+            ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
+            for (int hf = 0; hf < 2; ++hf)
+              ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
+                               64 * hf, c1, c2, batch);
+            ++issued;
+          }
+          // Let every copy this thread started land before the CTA can exit. On
+          // the normal path these phases have long completed; after an abort the
+          // consumer may never have waited for them.
+          dbg_ok(issued == 2 * n_kv || *abort_flag);  // every fill of the plan was issued
+          wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, false);
+          for (int s = 0; s < kStages && s < issued; ++s) {
+            const int fills = (issued - 1 - s) / kStages + 1;  // fills of stage s so far
+            wait_bounded(bar(kBarKvFull + s), (fills - 1) & 1, abort_flag, p.timeout_ns, false);
+          }
         }
       }
       __syncwarp();
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
-        const int n_kv = work_of<kCausal, kVarlen>(p).n_kv;
-        bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
-        ptx::tc_fence_after();
-        auto ring_wait = [&](int it) -> bool {
-          const bool r = wait_bounded(bar(kBarKvFull + it % kStages), (it / kStages) & 1, abort_flag,
-                                      p.timeout_ns, true);
-          ptx::tc_fence_after();
-          return r;
-        };
-        // Ring stage descriptors: K tiles are K-major B operands, V tiles MN-major.
-        auto k_desc = [&](int it) -> uint32_t {
-          return desc_lo(sRing + (it % kStages) * kTileBytes, 16);
-        };
-        auto v_desc = [&](int it) -> uint32_t {
-          return desc_lo(sRing + (it % kStages) * kTileBytes, kHalfBytes);
-        };
-        const uint32_t q0_desc = desc_lo(sQ, 16);
-        const uint32_t q1_desc = desc_lo(sQ + kTileBytes, 16);
-        if (ok) ok = ring_wait(0);
-        if (ok) {
-          issue_s(tmem + kTmemS0, q0_desc, k_desc(0));
-          if (!p.withhold_s0) ptx::mma_commit(bar(kBarSFull + 0));
-          issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(0));
-          ptx::mma_commit(bar(kBarSFull + 1));
-          ptx::mma_commit(bar(kBarKvEmpty + 0));
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int vit = 2 * j + 1;
-          const int kit = 2 * j + 2;
-          const bool more = j + 1 < n_kv;
-          if (!(ok = ring_wait(vit))) break;
-          if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
-          ptx::tc_fence_after();
-          const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
-          issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
-          if (!more) ptx::mma_commit(bar(kBarOFull + 0));
-          if (more) {
-            if (!(ok = ring_wait(kit))) break;
-            issue_s(tmem + kTmemS0, q0_desc, k_desc(kit));
-            ptx::mma_commit(bar(kBarSFull + 0));
-          }
-          if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
-          ptx::tc_fence_after();
-          issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
-          ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
-          if (!more) ptx::mma_commit(bar(kBarOFull + 1));
-          if (more) {
-            issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(kit));
+        if constexpr (kPersist) {
+          auto ring_wait = [&](int it) -> bool {
+            const bool r = wait_bounded(bar(kBarKvFull + it % kStages), (it / kStages) & 1, abort_flag,
+                                        p.timeout_ns, true);
+            ptx::tc_fence_after();
+            return r;
+          };
+          // Ring stage descriptors: K tiles are K-major B operands, V tiles MN-major.
+          auto k_desc = [&](int it) -> uint32_t {
+            return desc_lo(sRing + (it % kStages) * kTileBytes, 16);
+          };
+          auto v_desc = [&](int it) -> uint32_t {
+            return desc_lo(sRing + (it % kStages) * kTileBytes, kHalfBytes);
+          };
+          const uint32_t q0_desc = desc_lo(sQ, 16);
+          const uint32_t q1_desc = desc_lo(sQ + kTileBytes, 16);
+          bool ok = true;
+          int fill = 0;   // ring fills consumed by the items before this one
+          int ktile = 0;  // key tiles of the items before this one (S and P phases)
+          for (int item = blockIdx.x, iter = 0; ok && item < p.n_items; item += gridDim.x, ++iter) {
+            const int n_kv = work_of<kCausal, kVarlen>(p, item).n_kv;
+            if (!(ok = wait_bounded(bar(kBarQ), iter & 1, abort_flag, p.timeout_ns, true))) break;
+            ptx::tc_fence_after();
+            if (!(ok = ring_wait(fill))) break;
+            // S of the first key tile. The previous item's last P V MMAs, issued
+            // before these on the same pipe, have read the S/P columns first.
+            issue_s(tmem + kTmemS0, q0_desc, k_desc(fill));
+            if (!p.withhold_s0) ptx::mma_commit(bar(kBarSFull + 0));
+            issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(fill));
             ptx::mma_commit(bar(kBarSFull + 1));
-            ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+            ptx::mma_commit(bar(kBarKvEmpty + fill % kStages));
+            if (n_kv == 1) ptx::mma_commit(bar(kBarQFree));  // the item's last S MMAs
+            for (int j = 0; ok && j < n_kv; ++j) {
+              const int vit = fill + 2 * j + 1;
+              const int kit = fill + 2 * j + 2;
+              const bool more = j + 1 < n_kv;
+              if (!(ok = ring_wait(vit))) break;
+              if (!(ok = wait_bounded(bar(kBarPFull + 0), (ktile + j) & 1, abort_flag, p.timeout_ns, true)))
+                break;
+              // The first P V of an item starts a fresh partial in O: the previous
+              // item's epilogue must have read it.
+              if (j == 0 && iter > 0 &&
+                  !(ok = wait_bounded(bar(kBarOFree + 0), (iter - 1) & 1, abort_flag, p.timeout_ns, true)))
+                break;
+              ptx::tc_fence_after();
+              const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
+              issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
+              if (!more) ptx::mma_commit(bar(kBarOFull + 0));
+              if (more) {
+                if (!(ok = ring_wait(kit))) break;
+                issue_s(tmem + kTmemS0, q0_desc, k_desc(kit));
+                ptx::mma_commit(bar(kBarSFull + 0));
+              }
+              if (!(ok = wait_bounded(bar(kBarPFull + 1), (ktile + j) & 1, abort_flag, p.timeout_ns, true)))
+                break;
+              if (j == 0 && iter > 0 &&
+                  !(ok = wait_bounded(bar(kBarOFree + 1), (iter - 1) & 1, abort_flag, p.timeout_ns, true)))
+                break;
+              ptx::tc_fence_after();
+              issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
+              ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
+              if (!more) ptx::mma_commit(bar(kBarOFull + 1));
+              if (more) {
+                issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(kit));
+                ptx::mma_commit(bar(kBarSFull + 1));
+                ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+                if (j + 2 == n_kv) ptx::mma_commit(bar(kBarQFree));  // the item's last S MMAs
+              }
+            }
+            fill += 2 * n_kv;
+            ktile += n_kv;
+          }
+        } else {
+          const int n_kv = work_of<kCausal, kVarlen>(p).n_kv;
+          bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
+          ptx::tc_fence_after();
+          auto ring_wait = [&](int it) -> bool {
+            const bool r = wait_bounded(bar(kBarKvFull + it % kStages), (it / kStages) & 1, abort_flag,
+                                        p.timeout_ns, true);
+            ptx::tc_fence_after();
+            return r;
+          };
+          // Ring stage descriptors: K tiles are K-major B operands, V tiles MN-major.
+          auto k_desc = [&](int it) -> uint32_t {
+            return desc_lo(sRing + (it % kStages) * kTileBytes, 16);
+          };
+          auto v_desc = [&](int it) -> uint32_t {
+            return desc_lo(sRing + (it % kStages) * kTileBytes, kHalfBytes);
+          };
+          const uint32_t q0_desc = desc_lo(sQ, 16);
+          const uint32_t q1_desc = desc_lo(sQ + kTileBytes, 16);
+          if (ok) ok = ring_wait(0);
+          if (ok) {
+            issue_s(tmem + kTmemS0, q0_desc, k_desc(0));
+            if (!p.withhold_s0) ptx::mma_commit(bar(kBarSFull + 0));
+            issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(0));
+            ptx::mma_commit(bar(kBarSFull + 1));
+            ptx::mma_commit(bar(kBarKvEmpty + 0));
+          }
+          for (int j = 0; ok && j < n_kv; ++j) {
+            const int vit = 2 * j + 1;
+            const int kit = 2 * j + 2;
+            const bool more = j + 1 < n_kv;
+            if (!(ok = ring_wait(vit))) break;
+            if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
+            ptx::tc_fence_after();
+            const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
+            issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
+            if (!more) ptx::mma_commit(bar(kBarOFull + 0));
+            if (more) {
+              if (!(ok = ring_wait(kit))) break;
+              issue_s(tmem + kTmemS0, q0_desc, k_desc(kit));
+              ptx::mma_commit(bar(kBarSFull + 0));
+            }
+            if (!(ok = wait_bounded(bar(kBarPFull + 1), j & 1, abort_flag, p.timeout_ns, true))) break;
+            ptx::tc_fence_after();
+            issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
+            ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
+            if (!more) ptx::mma_commit(bar(kBarOFull + 1));
+            if (more) {
+              issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(kit));
+              ptx::mma_commit(bar(kBarSFull + 1));
+              ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+            }
           }
         }
         // Wait until every MMA issued so far has finished (immediate on the normal
@@ -705,188 +864,360 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = p.c;
     const bool pos = c >= 0.f;
     const float neg_inf = -__int_as_float(0x7F800000);
-    float m_used = neg_inf;
-    float l = 0.f;
-    Row acc;
+    if constexpr (kPersist) {
+      // One loop over every key tile of every item of this CTA (a loop over items
+      // around a loop over their tiles makes the compiler spill the row
+      // registers); an item's epilogue runs after its last tile.
+      bool ok = true;
+      int sp = 0;  // S and P phase parity (key tiles processed so far, mod 2)
+      int item = blockIdx.x;
+      int j = 0, n_kv = 0;
+      const int row_lim = 0;  // no per-row key limit on this path
+      float m_used = neg_inf, l = 0.f;
+      Row acc;
+      if (item < p.n_items) {
+        m_used = neg_inf;
+        l = 0.f;
 #pragma unroll
-    for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
-    bool ok = true;
-    int n_kv, row_lim;
-    {
+        for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+        n_kv = work_of<kCausal, kVarlen>(p, item).n_kv;  // key tiles of this item
+      }
+      while (ok && item < p.n_items) {
+        {
+            if (!(ok = warp_wait(bar(kBarSFull + t), sp, abort_flag, p.timeout_ns))) break;
+            ptx::tc_fence_after();
+            // The ragged key tile is the last tile of the last split. Written as tests
+            // of kernel parameters and the item index, which keeps the compiler's
+            // register allocation of this loop free of spills.
+            const bool last = (j == n_kv - 1) && (p.kv_tail < kBN) &&
+                              (!kPartial || item % p.n_splits == p.n_splits - 1);
+            // Masked tile: the ragged last tile; with the causal mask every tile, each
+            // row hiding the keys beyond its own limit (a tile it fully sees loses
+            // nothing). One path for all tiles keeps the loop's registers spill-free.
+            const bool masked = kRowLimit ? true : last;
+            constexpr int kM = kRowLimit ? kChunkMask : kElemMask;
+            const int valid = kRowLimit ? row_lim - kBN * j : p.kv_tail;
+            // Least `valid` over the warp (lane 0 has the warp's first row).
+            const int vmin = kRowLimit ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
+            // Pass A: take the row extreme of S_j and, on a fold tile, add the TMEM
+            // partial into the row (it holds the tiles since the last fold, complete
+            // because the MMA that wrote S_j was issued after PV_{j-1}, and PV_j waits
+            // for P_j).
+            float ext, m_tile;
+            bool need;
+            if constexpr (kFoldOf<kPartial> == 1) {
+              if (pos) {
+                if (j == 0) {
+                  ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                               : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+                } else {
+                  ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                               : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+                }
+              } else {
+                ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
+                             : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
+              }
+              m_tile = ext * c;
+              need = m_tile > m_used + kTau;  // false for NaN
+              if (need) {
+                const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+                if (j > 0) rescale_row(acc, f);
+                l *= f;
+                m_used = m_tile;
+              }
+            } else {
+              // The TMEM partial (key tiles since the last fold) is folded into the
+              // registers every kFoldOf<kPartial> tiles.
+              const bool fold_now = j > 0 && (j % kFoldOf<kPartial>) == 0;
+              if (pos) {
+                if (!fold_now) {
+                  ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                               : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+                } else {
+                  ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                               : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+                }
+              } else {
+                ext = masked ? fold_and_min<true>(tS, tO, acc, valid, fold_now)
+                             : fold_and_min<false>(tS, tO, acc, kBN, fold_now);
+              }
+              m_tile = ext * c;
+              need = m_tile > m_used + kTau;  // false for NaN
+              float f_row = 1.f;  // this row's rescale factor at this tile
+              if (need) {
+                const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+                if (j > 0) rescale_row(acc, f);
+                l *= f;
+                m_used = m_tile;
+                f_row = f;
+              }
+              // A partial still in TMEM is relative to the old reference: scale it in
+              // place (the PV MMAs that wrote it are done, S_j being ready; the next one
+              // waits for P_j). Warp-uniform: each lane rescales its own row, by 1 if its
+              // reference did not move.
+              if ((j % kFoldOf<kPartial>) != 0 && __any_sync(0xFFFFFFFFu, need))
+                rescale_tmem_row(tO, f_row);
+            }
+            const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
+            // Causal, c > 0: pass A left -Inf in the hidden columns, so pass B needs
+            // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
+            const bool masked_b = kRowLimit ? !(c > 0.f) : last;
+            if (kRowLimit) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
+            l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(kBarPFull + t));
+        }
+        sp ^= 1;
+        if (++j < n_kv) continue;
+        // ---- the item's epilogue
+        const int iter = (item - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
+        if (!(ok = warp_wait(bar(kBarOFull + t), iter & 1, abort_flag, p.timeout_ns))) break;
+        // Fold the last partial into the row, then hand O back to the tensor pipe
+        // (the next item's first P V overwrites it) before the stores.
+        ptx::tc_fence_after();
+        fold_last(tO, acc);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kBarOFree + t));
+        // Normalise, round, and store this warp's 32 rows with two TMA boxes (one
+        // per 64-column half) through its 4 KiB staging buffer, in the 128-byte
+        // swizzle. A buffer is rewritten only after the previous box has been
+        // read out of it; rows past Sq are clipped by the store.
+        const Work wk = work_of<kCausal, kVarlen>(p, item);
+        const uint32_t stage_w = sbase + kOffStage + (t * 4 + wq) * kStageWarpBytes;
+        const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;
+        const uint32_t bias = p.mode == 0 ? 0x7FFFu : (p.mode == 1 ? 0x8000u : 0u);
+        const uint32_t lsb_mask = p.mode == 0 ? 1u : 0u;
+        const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
+        const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (lane == 0) ptx::bulk_wait_group_read_0();
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float o0, o1;
+              ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+              w[i] = round_bf16_biased(o0, bias, lsb_mask) | (round_bf16_biased(o1, bias, lsb_mask) << 16);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int chunk = ch * 4 + u;
+              ptx::st_shared_v4(stage_w + lane * 128 + ((chunk ^ (lane & 7)) << 4), w[4 * u],
+                                w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && q_row0 < p.Sq && dbg_ok(q_row0 >= 0)) {
+            int c1, c2;
+            tma_coords(p.layout, q_row0, wk.head, c1, c2);
+            ptx::tma_store_4d(&tm_o, stage_w, 64 * hf, c1, c2, wk.batch);
+            ptx::bulk_commit_group();
+          }
+        }
+        item += gridDim.x;
+        j = 0;
+        if (item < p.n_items) {
+          m_used = neg_inf;
+          l = 0.f;
+#pragma unroll
+          for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+          n_kv = work_of<kCausal, kVarlen>(p, item).n_kv;  // key tiles of this item
+        }
+      }
+      // Every store of this warp has completed before the CTA can exit.
+      if (lane == 0) ptx::bulk_wait_group_0();
+      __syncwarp();
+    } else {
+      float m_used = neg_inf;
+      float l = 0.f;
+      Row acc;
+#pragma unroll
+      for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+      bool ok = true;
+      int n_kv, row_lim;
+      {
+        const Work wk = work_of<kCausal, kVarlen>(p);
+        n_kv = wk.n_kv;  // key tiles of this CTA
+        // Number of keys this row sees, counted from the sequence's key 0: the
+        // causal limit (capped at Sk, which also hides the ragged tail from the
+        // padding rows past Sq), or for a variable-length batch without the mask
+        // the sequence's key count (hiding the next sequence's keys).
+        row_lim = kCausal ? min((2 * wk.pair + t) * kBM + row + (wk.sk - wk.sq) + 1, wk.sk)
+                          : (kVarlen ? wk.sk : 0);
+      }
+
+      for (int j = 0; j < n_kv; ++j) {
+        if (!(ok = warp_wait(bar(kBarSFull + t), j & 1, abort_flag, p.timeout_ns))) break;
+        ptx::tc_fence_after();
+        // The ragged key tile is the last tile of the last split. Written as tests
+        // of kernel parameters and the block index, which keeps the compiler's
+        // register allocation of this loop free of spills.
+        const bool last = (j == n_kv - 1) && (p.kv_tail < kBN) &&
+                          (!kPartial || static_cast<int>(blockIdx.x % p.n_splits) == p.n_splits - 1);
+        // Masked tile: the ragged last tile; with the causal mask every tile, each
+        // row hiding the keys beyond its own limit (a tile it fully sees loses
+        // nothing). One path for all tiles keeps the loop's registers spill-free.
+        const bool masked = kRowLimit ? true : last;
+        constexpr int kM = kRowLimit ? kChunkMask : kElemMask;
+        const int valid = kRowLimit ? row_lim - kBN * j : p.kv_tail;
+        // Least `valid` over the warp (lane 0 has the warp's first row).
+        const int vmin = kRowLimit ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
+        // Pass A: take the row extreme of S_j and, on a fold tile, add the TMEM
+        // partial into the row (it holds the tiles since the last fold, complete
+        // because the MMA that wrote S_j was issued after PV_{j-1}, and PV_j waits
+        // for P_j).
+        float ext, m_tile;
+        bool need;
+        if constexpr (kFoldOf<kPartial> == 1) {
+          if (pos) {
+            if (j == 0) {
+              ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                           : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+            } else {
+              ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                           : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+            }
+          } else {
+            ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
+                         : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
+          }
+          m_tile = ext * c;
+          need = m_tile > m_used + kTau;  // false for NaN
+          if (need) {
+            const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+            if (j > 0) rescale_row(acc, f);
+            l *= f;
+            m_used = m_tile;
+          }
+        } else {
+          // The TMEM partial (key tiles since the last fold) is folded into the
+          // registers every kFoldOf<kPartial> tiles.
+          const bool fold_now = j > 0 && (j % kFoldOf<kPartial>) == 0;
+          if (pos) {
+            if (!fold_now) {
+              ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
+                           : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
+            } else {
+              ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
+                           : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+            }
+          } else {
+            ext = masked ? fold_and_min<true>(tS, tO, acc, valid, fold_now)
+                         : fold_and_min<false>(tS, tO, acc, kBN, fold_now);
+          }
+          m_tile = ext * c;
+          need = m_tile > m_used + kTau;  // false for NaN
+          float f_row = 1.f;  // this row's rescale factor at this tile
+          if (need) {
+            const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+            if (j > 0) rescale_row(acc, f);
+            l *= f;
+            m_used = m_tile;
+            f_row = f;
+          }
+          // A partial still in TMEM is relative to the old reference: scale it in
+          // place (the PV MMAs that wrote it are done, S_j being ready; the next one
+          // waits for P_j). Warp-uniform: each lane rescales its own row, by 1 if its
+          // reference did not move.
+          if ((j % kFoldOf<kPartial>) != 0 && __any_sync(0xFFFFFFFFu, need))
+            rescale_tmem_row(tO, f_row);
+        }
+        const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
+        // Causal, c > 0: pass A left -Inf in the hidden columns, so pass B needs
+        // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
+        const bool masked_b = kRowLimit ? !(c > 0.f) : last;
+        if (kRowLimit) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
+        l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kBarPFull + t));
+      }
+
+      if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
       const Work wk = work_of<kCausal, kVarlen>(p);
-      n_kv = wk.n_kv;  // key tiles of this CTA
-      // Number of keys this row sees, counted from the sequence's key 0: the
-      // causal limit (capped at Sk, which also hides the ragged tail from the
-      // padding rows past Sq), or for a variable-length batch without the mask
-      // the sequence's key count (hiding the next sequence's keys).
-      row_lim = kCausal ? min((2 * wk.pair + t) * kBM + row + (wk.sk - wk.sq) + 1, wk.sk)
-                        : (kVarlen ? wk.sk : 0);
-    }
-
-    for (int j = 0; j < n_kv; ++j) {
-      if (!(ok = warp_wait(bar(kBarSFull + t), j & 1, abort_flag, p.timeout_ns))) break;
-      ptx::tc_fence_after();
-      // The ragged key tile is the last tile of the last split. Written as tests
-      // of kernel parameters and the block index, which keeps the compiler's
-      // register allocation of this loop free of spills.
-      const bool last = (j == n_kv - 1) && (p.kv_tail < kBN) &&
-                        (!kPartial || static_cast<int>(blockIdx.x % p.n_splits) == p.n_splits - 1);
-      // Masked tile: the ragged last tile; with the causal mask every tile, each
-      // row hiding the keys beyond its own limit (a tile it fully sees loses
-      // nothing). One path for all tiles keeps the loop's registers spill-free.
-      const bool masked = kRowLimit ? true : last;
-      constexpr int kM = kRowLimit ? kChunkMask : kElemMask;
-      const int valid = kRowLimit ? row_lim - kBN * j : p.kv_tail;
-      // Least `valid` over the warp (lane 0 has the warp's first row).
-      const int vmin = kRowLimit ? __shfl_sync(0xFFFFFFFFu, valid, 0) : p.kv_tail;
-      // Pass A: take the row extreme of S_j and, on a fold tile, add the TMEM
-      // partial into the row (it holds the tiles since the last fold, complete
-      // because the MMA that wrote S_j was issued after PV_{j-1}, and PV_j waits
-      // for P_j).
-      float ext, m_tile;
-      bool need;
-      if constexpr (kFoldOf<kPartial> == 1) {
-        if (pos) {
-          if (j == 0) {
-            ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
-                         : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
-          } else {
-            ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
-                         : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+      if (kPartial && ok) {
+        // Split epilogue: this row's unnormalised fp32 output, the running max it is
+        // relative to, and its row sum.
+        ptx::tc_fence_after();
+        fold_last(tO, acc);
+        const int q = (2 * wk.pair + t) * kBM + row;
+        if (q < p.Sq) {
+          const size_t r = (static_cast<size_t>(wk.split) * p.BH + wk.bh) * p.sq_pad + q;
+          if (dbg_ok(r < static_cast<size_t>(p.n_splits) * p.BH * p.sq_pad)) {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + r * kD);
+#pragma unroll
+            for (int i = 0; i < kD / 4; ++i) {
+              float a0, a1, a2, a3;
+              ptx::f2_unpack(acc[2 * i], a0, a1);
+              ptx::f2_unpack(acc[2 * i + 1], a2, a3);
+              dst[i] = make_float4(a0, a1, a2, a3);
+            }
+            // The products are relative to m_used, or to 0 while it is -Inf (then no
+            // key had a finite logit and both sums are 0, or NaN).
+            reinterpret_cast<float2*>(p.part_rl)[r] = make_float2(m_used, l);
           }
-        } else {
-          ext = masked ? fold_and_min<true>(tS, tO, acc, valid, j > 0)
-                       : fold_and_min<false>(tS, tO, acc, kBN, j > 0);
         }
-        m_tile = ext * c;
-        need = m_tile > m_used + kTau;  // false for NaN
-        if (need) {
-          const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
-          if (j > 0) rescale_row(acc, f);
-          l *= f;
-          m_used = m_tile;
-        }
-      } else {
-        // The TMEM partial (key tiles since the last fold) is folded into the
-        // registers every kFoldOf<kPartial> tiles.
-        const bool fold_now = j > 0 && (j % kFoldOf<kPartial>) == 0;
-        if (pos) {
-          if (!fold_now) {
-            ext = masked ? fold_and_max<kM, false>(tS, tO, acc, valid, vmin)
-                         : fold_and_max<kNoMask, false>(tS, tO, acc, kBN, kBN);
-          } else {
-            ext = masked ? fold_and_max<kM, true>(tS, tO, acc, valid, vmin)
-                         : fold_and_max<kNoMask, true>(tS, tO, acc, kBN, kBN);
+      } else if (ok) {
+        ptx::tc_fence_after();
+        fold_last(tO, acc);
+        // Normalise, round, stage in the (now free) Q tile buffer with the TMA
+        // 128-byte swizzle, and store this warp's 32 rows with two TMA boxes.
+        const uint32_t stage_base = sQ + t * kTileBytes;
+        const int mode = p.mode;
+        const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
+        const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float o0, o1;
+            ptx::f2_unpack(ptx::f2_mul(acc[16 * ch + i], inv2), o0, o1);
+            w[i] = round_bf16_bits(o0, mode) | (round_bf16_bits(o1, mode) << 16);
           }
-        } else {
-          ext = masked ? fold_and_min<true>(tS, tO, acc, valid, fold_now)
-                       : fold_and_min<false>(tS, tO, acc, kBN, fold_now);
-        }
-        m_tile = ext * c;
-        need = m_tile > m_used + kTau;  // false for NaN
-        float f_row = 1.f;  // this row's rescale factor at this tile
-        if (need) {
-          const float f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
-          if (j > 0) rescale_row(acc, f);
-          l *= f;
-          m_used = m_tile;
-          f_row = f;
-        }
-        // A partial still in TMEM is relative to the old reference: scale it in
-        // place (the PV MMAs that wrote it are done, S_j being ready; the next one
-        // waits for P_j). Warp-uniform: each lane rescales its own row, by 1 if its
-        // reference did not move.
-        if ((j % kFoldOf<kPartial>) != 0 && __any_sync(0xFFFFFFFFu, need))
-          rescale_tmem_row(tO, f_row);
-      }
-      const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
-      // Causal, c > 0: pass A left -Inf in the hidden columns, so pass B needs
-      // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
-      const bool masked_b = kRowLimit ? !(c > 0.f) : last;
-      if (kRowLimit) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
-      l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kBarPFull + t));
-    }
-
-    if (ok) ok = warp_wait(bar(kBarOFull + t), 0, abort_flag, p.timeout_ns);
-    const Work wk = work_of<kCausal, kVarlen>(p);
-    if (kPartial && ok) {
-      // Split epilogue: this row's unnormalised fp32 output, the running max it is
-      // relative to, and its row sum.
-      ptx::tc_fence_after();
-      fold_last(tO, acc);
-      const int q = (2 * wk.pair + t) * kBM + row;
-      if (q < p.Sq) {
-        const size_t r = (static_cast<size_t>(wk.split) * p.BH + wk.bh) * p.sq_pad + q;
-        if (dbg_ok(r < static_cast<size_t>(p.n_splits) * p.BH * p.sq_pad)) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + r * kD);
+          const uint32_t half_base = stage_base + (ch >> 1) * kHalfBytes + row * 128;
 #pragma unroll
-          for (int i = 0; i < kD / 4; ++i) {
-            float a0, a1, a2, a3;
-            ptx::f2_unpack(acc[2 * i], a0, a1);
-            ptx::f2_unpack(acc[2 * i + 1], a2, a3);
-            dst[i] = make_float4(a0, a1, a2, a3);
+          for (int u = 0; u < 4; ++u) {
+            const int chunk = (ch & 1) * 4 + u;
+            ptx::st_shared_v4(half_base + ((chunk ^ (row & 7)) << 4), w[4 * u], w[4 * u + 1],
+                              w[4 * u + 2], w[4 * u + 3]);
           }
-          // The products are relative to m_used, or to 0 while it is -Inf (then no
-          // key had a finite logit and both sums are 0, or NaN).
-          reinterpret_cast<float2*>(p.part_rl)[r] = make_float2(m_used, l);
         }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;  // within the sequence
+        if (!kVarlen || q_row0 + 32 <= wk.sq) {
+          if (lane == 0 && q_row0 < wk.sq && dbg_ok(wk.q_base + q_row0 < p.Sq)) {
+            int c1, c2;
+            tma_coords(p.layout, wk.q_base + q_row0, wk.head, c1, c2);
+            for (int hf = 0; hf < 2; ++hf)
+              ptx::tma_store_4d(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1, c2,
+                                wk.batch);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_0();
+          }
+        } else if (lane < wk.sq - q_row0 && dbg_ok(wk.q_base + q_row0 + lane < p.Sq)) {
+          // The sequence ends inside this warp's rows: a TMA box would run into the
+          // next sequence's rows, so each row up to the end is copied out of the
+          // staging buffer with plain 16-byte stores (packed layout: token, head).
+          const uint8_t* stage = smem + (stage_base - sbase);
+          uint4* dst = reinterpret_cast<uint4*>(
+              p.out + (static_cast<size_t>(wk.q_base + q_row0 + lane) * p.H + wk.head) * kD);
+#pragma unroll
+          for (int cix = 0; cix < 16; ++cix) {
+            const int off = (cix >> 3) * kHalfBytes + row * 128 + (((cix & 7) ^ (row & 7)) << 4);
+            dst[cix] = *reinterpret_cast<const uint4*>(stage + off);
+          }
+        }
+        __syncwarp();
       }
-    } else if (ok) {
-      ptx::tc_fence_after();
-      fold_last(tO, acc);
-      // Normalise, round, stage in the (now free) Q tile buffer with the TMA
-      // 128-byte swizzle, and store this warp's 32 rows with two TMA boxes.
-      const uint32_t stage_base = sQ + t * kTileBytes;
-      const int mode = p.mode;
-      const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
-      const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float o0, o1;
-          ptx::f2_unpack(ptx::f2_mul(acc[16 * ch + i], inv2), o0, o1);
-          w[i] = round_bf16_bits(o0, mode) | (round_bf16_bits(o1, mode) << 16);
-        }
-        const uint32_t half_base = stage_base + (ch >> 1) * kHalfBytes + row * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = (ch & 1) * 4 + u;
-          ptx::st_shared_v4(half_base + ((chunk ^ (row & 7)) << 4), w[4 * u], w[4 * u + 1],
-                            w[4 * u + 2], w[4 * u + 3]);
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;  // within the sequence
-      if (!kVarlen || q_row0 + 32 <= wk.sq) {
-        if (lane == 0 && q_row0 < wk.sq && dbg_ok(wk.q_base + q_row0 < p.Sq)) {
-          int c1, c2;
-          tma_coords(p.layout, wk.q_base + q_row0, wk.head, c1, c2);
-          for (int hf = 0; hf < 2; ++hf)
-            ptx::tma_store_4d(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1, c2,
-                              wk.batch);
-          ptx::bulk_commit_group();
-          ptx::bulk_wait_group_0();
-        }
-      } else if (lane < wk.sq - q_row0 && dbg_ok(wk.q_base + q_row0 + lane < p.Sq)) {
-        // The sequence ends inside this warp's rows: a TMA box would run into the
-        // next sequence's rows, so each row up to the end is copied out of the
-        // staging buffer with plain 16-byte stores (packed layout: token, head).
-        const uint8_t* stage = smem + (stage_base - sbase);
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + (static_cast<size_t>(wk.q_base + q_row0 + lane) * p.H + wk.head) * kD);
-#pragma unroll
-        for (int cix = 0; cix < 16; ++cix) {
-          const int off = (cix >> 3) * kHalfBytes + row * 128 + (((cix & 7) ^ (row & 7)) << 4);
-          dst[cix] = *reinterpret_cast<const uint4*>(stage + off);
-        }
-      }
-      __syncwarp();
+  
     }
   }
 

@@ -93,6 +93,13 @@ __device__ __forceinline__ void bulk_wait_group_0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Waits until every committed bulk store of the thread has read its shared
+// memory source (the buffer may then be rewritten; the writes may still be in
+// flight).
+__device__ __forceinline__ void bulk_wait_group_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_slot),
