@@ -258,13 +258,19 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
   return u >> 16;
 }
 
-// round_bf16_bits with the mode's constants hoisted out of the element loop: one
-// add before the truncation, bias 0x7FFF plus the kept lowest bit (lsb_mask 1)
-// for RTNE, 0x8000 for RTNA, 0 for RTZ; NaN gives the one pattern 0x7FC0.
-__device__ __forceinline__ uint32_t round_bf16_biased(float x, uint32_t bias, uint32_t lsb_mask) {
-  const uint32_t u = __float_as_uint(x);
-  const uint32_t r = (u + bias + ((u >> 16) & lsb_mask)) >> 16;
-  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC0u : r;
+// Two fp32 results of arithmetic -> packed bf16x2 (x0 in bits 0..15), rounded as
+// round_bf16_bits does, with the mode's constants hoisted out of the element
+// loop: bias 0x7FFF plus the kept lowest bit (lsb_mask 1) for RTNE, 0x8000 for
+// RTNA, 0 for RTZ, added before the upper halves are taken. A NaN produced by
+// fp32 arithmetic on this GPU is the positive pattern 0x7FFFFFFF: as a signed
+// integer it is above 0x7FC00000, so a signed min turns it (and only it: every
+// other value, negative ones included, is not above) into 0x7FC00000, which
+// every mode rounds to the one NaN pattern 0x7FC0.
+__device__ __forceinline__ uint32_t round_pair_bf16(float x0, float x1, uint32_t bias,
+                                                    uint32_t lsb_mask) {
+  const uint32_t u0 = static_cast<uint32_t>(min(__float_as_int(x0), 0x7FC00000));
+  const uint32_t u1 = static_cast<uint32_t>(min(__float_as_int(x1), 0x7FC00000));
+  return ptx::prmt_hi16(u0 + bias + ((u0 >> 16) & lsb_mask), u1 + bias + ((u1 >> 16) & lsb_mask));
 }
 
 // The running output row of a softmax thread: 128 fp32 as 64 packed pairs
@@ -1002,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i) {
               float o0, o1;
               ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
-              w[i] = round_bf16_biased(o0, bias, lsb_mask) | (round_bf16_biased(o1, bias, lsb_mask) << 16);
+              w[i] = round_pair_bf16(o0, o1, bias, lsb_mask);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {

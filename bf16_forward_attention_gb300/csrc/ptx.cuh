@@ -396,6 +396,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return y;
 }
 
+// The upper 16 bits of a (into bits 0..15) and of b (into bits 16..31).
+__device__ __forceinline__ uint32_t prmt_hi16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
