@@ -79,6 +79,11 @@ enum {
  * reached the call. All pointers must be 16-byte aligned. The call allocates
  * no device memory. Results are bit-identical from run to run. Thread-safe.
  * Returns ATTN_OK or a negative status code.
+ *
+ * Schedule (invisible in the result): one CTA per (batch, head, pair of
+ * 128-row query tiles); when Sk <= 2048 and there are more such items than
+ * SMs, one CTA per SM loops over them instead, overlapping each item's loads
+ * and stores with its neighbours'.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
              int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,

@@ -52,6 +52,14 @@ def test_base_and_causal_gqa(monkeypatch, layout, Sq, Sk):
     _same(*_both(monkeypatch, lambda: attn.attn_fwd_ex(q, k, v, causal=True, layout=layout)))
 
 
+@pytest.mark.parametrize("layout", ["bhsd", "bshd"])
+def test_persistent_short_keys(monkeypatch, layout):
+    # 2 x 96 heads x 2 query-tile pairs = 384 items (more than the SMs) over 3 key
+    # tiles: the persistent variant, one CTA per SM looping over items.
+    q, k, v = _qkv(layout, 2, 96, 96, 500, 300, seed=1405)
+    _same(*_both(monkeypatch, lambda: attn.attn_fwd(q, k, v, layout=layout)))
+
+
 def test_split_kv(monkeypatch):
     q, k, v = _qkv("bhsd", 1, 2, 2, 256, 5000, seed=1410)
     _same(*_both(monkeypatch, lambda: attn.attn_fwd_splitkv(q, k, v, num_splits=5)))
