@@ -22,6 +22,12 @@
 // softmax runs (the pages' "keep the matrix core busy while softmax and loads
 // overlap", section "Hvordan kernen arbejder").
 //
+// The persistent variant (short key ranges) runs one CTA per SM over many such
+// items with the same roles, carrying every barrier phase from item to item:
+// the next item's Q loads as soon as the current item's last S MMAs are done,
+// and each softmax warp stores its rows through a 4 KiB staging buffer of its
+// own rather than through the Q buffer.
+//
 // Softmax is the online (running-max) form in base 2 with a lazy rescale: the
 // running output and row sum are rescaled only when a tile's max exceeds the max
 // in use by more than kTau (log2 units). P is written back into the S columns as
