@@ -79,11 +79,12 @@ def test_persistent_specials_and_negative_scale():
     kb[0, 11, 3, 9] = 0x7F80  # +Inf key element in head 11
     for scale in (inputs.default_scale(), -0.04):
         exact = attention_fp64(f64_of(q), f64_of(k), f64_of(v), scale, layout)
-        out = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), layout=layout, rounding="rtz",
-                            scale=scale)
-        torch.cuda.synchronize()
-        assert attn.attn_fwd_last_error() == attn.ATTN_OK
-        assert_parity(compare(bits_of(out), exact, "rtz"), max_abs_err=None)
+        for mode in inputs.ROUNDINGS:  # every mode writes NaN as the one pattern 0x7FC0
+            out = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), layout=layout, rounding=mode,
+                                scale=scale)
+            torch.cuda.synchronize()
+            assert attn.attn_fwd_last_error() == attn.ATTN_OK
+            assert_parity(compare(bits_of(out), exact, mode), max_abs_err=None)
 
 
 def test_persistent_equals_one_cta_per_item_bitwise():
