@@ -1,19 +1,26 @@
 """Benchmark: bf16 forward attention on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload self8k|cross4k32k|long128k|stress16381|tiny|decode32k|causal8k|gqa8k|varlen16]
+                    [--workload long128k|self8k|cross4k32k|stress16381|tiny|decode32k|causal8k|
+                                gqa8k|varlen16|short77]
 
-Workload (default): self-attention, BSHD, B=2, H=16, Sq=Sk=8192, d=128, bf16
-Q/K/V ~ N(0,1) from a fixed seed, scale 1/sqrt(128). One step = one call of the
-fused kernel per output rounding mode (RTNE, RTNA, RTZ) over the same inputs.
-Metric: TFLOP/s counted as 4*B*H*Sq*Sk*d per call, and the fraction of the
-measured dense bf16 peak. Inputs (192 MiB) exceed the 129 MB L2; L2 is not
-flushed between steps.
+Workload (default): long-context self-attention, BSHD, B=1, H=8,
+Sq=Sk=131072, d=128, bf16 Q/K/V ~ N(0,1) from a fixed seed, scale 1/sqrt(128),
+RTNA output rounding: the largest single-GPU shape. One step = one call of the
+fused kernel per output rounding mode of the workload over the same inputs
+(self8k runs RTNE, RTNA and RTZ). Metric: TFLOP/s counted as 4*B*H*Sq*Sk*d per
+call, and the fraction of the measured dense bf16 peak. Inputs (768 MiB) exceed
+the 129 MB L2; L2 is not flushed between steps. Besides the K timed steps, at
+least 100 further launches are timed one by one for the launch-time
+distribution (median, p5, p95).
 
 --impl reference times the fp64 CPU oracle (test infrastructure) on the host cores
 on a bounded sample of the same workload, in the same unit.
-Under torchrun (N > 1) every rank runs its own copy of the workload on its own GPU
-(weak scaling, no data exchange); rank 0 prints the max-over-ranks timing.
+With N > 1 every rank runs its own copy of the workload on its own GPU (weak
+scaling, no data exchange); rank 0 prints the max-over-ranks timing. Ranks come
+from torchrun (RANK / WORLD_SIZE / LOCAL_RANK in the environment) or, when those
+are unset, from N processes that bench.py starts itself (rendezvous on
+127.0.0.1).
 """
 from __future__ import annotations
 
@@ -116,6 +123,41 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def _free_port() -> int:
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _replica_entry(rank: int, world: int, port: int, target, target_args):
+    """One replica rank: the environment torchrun would have set, then target."""
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    rc = target(*target_args)
+    sys.stdout.flush()
+    if rc:
+        raise SystemExit(rc)
+
+
+def run_replicas(world: int, target, target_args=()) -> int:
+    """Starts `world` processes (spawned, so none inherits a CUDA context), rank r
+    on GPU r, each calling target(*target_args) with the torchrun environment set.
+    Returns 0 if every rank exited 0, else 1."""
+    import torch.multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_replica_entry, args=(r, world, port, target, target_args))
+             for r in range(world)]
+    for pr in procs:
+        pr.start()
+    for pr in procs:
+        pr.join()
+    return 0 if all(pr.exitcode == 0 for pr in procs) else 1
 
 
 def max_over_ranks(x: float, dist, device=None) -> float:
@@ -317,7 +359,7 @@ def run_reference(args, w):
     value = sum(f for f, _, _ in done) / t_total / 1e12
     rows = sum(r for _, _, r in done)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / max(1, len(done)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": _config(w, world),
@@ -420,6 +462,25 @@ def run_ours(args, w):
         dist.destroy_process_group()
         return 0
 
+    # Launch-time distribution: the timed launches, plus single launches timed one
+    # by one until there are at least --dist-launches of them (outside the timed
+    # region; value and roofline use the timed region only).
+    dist_ms = list(launch_ms)
+    extra = max(0, args.dist_launches - len(dist_ms))
+    if extra:
+        evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(extra)]
+        for i in range(extra):
+            m = w.roundings[i % len(w.roundings)]
+            evx[i][0].record(stream)
+            call(q, k, v, m, outs[m])
+            evx[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        dist_ms += [a.elapsed_time(b) for a, b in evx]
+        if attn.attn_fwd_last_error() != attn.ATTN_OK:
+            raise RuntimeError("a device-side wait timed out in the distribution launches")
+    dist_ms.sort()
+
     # End to end through the public API, everything inside the timed region:
     # attn_fwd_host (attn_fwd_varlen_host for a packed batch), the C ABI's
     # host-buffer entries (pinned host inputs in, pinned host output back, the
@@ -511,9 +572,10 @@ def run_ours(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": _config(w, world),
         "pct_of_dense_bf16_peak": 100.0 * tflops_launch / peak,
-        "launch_ms": {"median": launch_ms[len(launch_ms) // 2],
-                      "p5": launch_ms[int(0.05 * (len(launch_ms) - 1))],
-                      "p95": launch_ms[int(0.95 * (len(launch_ms) - 1))], "n": len(launch_ms)},
+        "launch_ms": {"median": dist_ms[len(dist_ms) // 2],
+                      "p5": dist_ms[int(0.05 * (len(dist_ms) - 1))],
+                      "p95": dist_ms[int(0.95 * (len(dist_ms) - 1))], "n": len(dist_ms),
+                      "timed_region_mean": avg_launch_ms, "timed_region_n": len(launch_ms)},
         "roofline": {"bound": bound, "achieved": achieved, "peak": roof_peak, "unit": roof_unit,
                      "frac": achieved / roof_peak,
                      "traffic": args.traffic if args.traffic is not None else _recorded_traffic(w.name),
@@ -543,21 +605,27 @@ def run_ours(args, w):
     return 0
 
 
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="self8k")
+    ap.add_argument("--workload", default="long128k")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=None,
                     help="fp64 CPU seconds per reference step (default: a 150 s budget for "
                          "the whole run over warmup + steps, 0.5..10 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dist-launches", type=int, default=100,
+                    help="launches timed one by one, after the timed steps, for the launch-time "
+                         "distribution (at least the timed launches are used if more)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the kernel, from an ncu capture")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # No launcher: start the replica ranks here (one process per GPU).
+        return run_replicas(args.gpus, main, (argv if argv is not None else sys.argv[1:],))
     if args.impl == "ours" and args.warmup < 3:
         args.warmup = 3
     from bf16_forward_attention_gb300 import inputs

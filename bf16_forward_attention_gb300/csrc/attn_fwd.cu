@@ -414,8 +414,12 @@ int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64
   if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || num_splits < 1) return ATTN_ERR_INVALID_ARG;
   if (d != 128) return ATTN_ERR_UNSUPPORTED;
   if (num_splits > kv_tiles_of(Sk)) return ATTN_ERR_INVALID_ARG;
-  if (B > (int64_t(1) << 31) || H > (int64_t(1) << 31) || Sq > (int64_t(1) << 31))
-    return ATTN_ERR_TOO_LARGE;
+  // The launch's own limits, checked before anything is multiplied: every
+  // factor below 2^31 and at most 2^31 - 1 CTAs (batch x head x query-tile pair
+  // x split), so the byte count below stays under 2^31 * 256 * 520 < 2^48.
+  const int64_t kLim31 = (int64_t(1) << 31) - 1;
+  if (B > kLim31 || H > kLim31 || Sq > kLim31 || Sk > kLim31) return ATTN_ERR_TOO_LARGE;
+  if (B * H > kLim31 / qpairs_of(Sq) / num_splits) return ATTN_ERR_TOO_LARGE;
   if (num_splits == 1) return 0;
   return splitkv_bytes(B, H, Sq, num_splits);
 }
@@ -502,7 +506,10 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
                                         void* stream) {
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   const int64_t need = attn_fwd_splitkv_workspace_bytes(B, H, Sq, Sk, d, num_splits);
-  if (need < 0) return static_cast<int>(need);
+  // A negative size is one of the status codes above; pass on only those.
+  if (need == ATTN_ERR_INVALID_ARG || need == ATTN_ERR_UNSUPPORTED || need == ATTN_ERR_TOO_LARGE)
+    return static_cast<int>(need);
+  if (need < 0) return ATTN_ERR_TOO_LARGE;
   if (need > kNoAllocScratchBytes) return ATTN_ERR_SCRATCH;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -174,7 +174,11 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
                     void* stream);
 
 /* Workspace bytes attn_fwd_splitkv needs (0 for num_splits == 1), or a negative
- * status code for invalid sizes. Host only. */
+ * status code: ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED for invalid sizes,
+ * ATTN_ERR_TOO_LARGE when a size exceeds 2^31 - 1 or the launch would need more
+ * than 2^31 - 1 CTAs (B * H * ceil(Sq / 256) * num_splits). The limits are
+ * checked before any product is formed, so the result never overflows. Host
+ * only. */
 int64_t attn_fwd_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d,
                                          int num_splits);
 
@@ -200,7 +204,9 @@ int attn_fwd_splitkv_num_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk);
  *     32 MiB is rejected with ATTN_ERR_SCRATCH before anything is launched.
  *   - The first call on a device looks up the array's device address for that
  *     device (cudaGetSymbolAddress); make that first call before any stream
- *     capture.
+ *     capture. The address is kept for the life of the process: after a
+ *     cudaDeviceReset of that device the library's device memory is gone, and
+ *     this entry point must not be called on that device again.
  *   - Every call on a device shares the one array, and each call overwrites the
  *     part it uses before reading it (nothing has to start at zero). Calls that
  *     overlap in time on the GPU, from any stream or thread, race on it: order

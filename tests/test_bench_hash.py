@@ -26,7 +26,20 @@ def test_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.kernel_sources_hash() != h0
 
 
-def test_recorded_traffic_matches_current_sources():
-    # The committed record must belong to the committed kernel code.
+def test_recorded_traffic_is_used_only_for_the_code_it_was_taken_on(tmp_path, monkeypatch):
+    # A DRAM record counts only while the kernel code it was captured on is the
+    # current code; otherwise the bench line reports traffic as null.
+    import json
     bench = _bench()
-    assert bench._recorded_traffic("self8k") is not None
+    src = tmp_path / "k.cuh"
+    src.write_text("int f() { return 1; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", ("k.cuh",))
+    (tmp_path / "profiles").mkdir()
+    rec = {"attn_fwd_kernel": {"long128k": {"sources_sha256_16": bench.kernel_sources_hash(),
+                                            "dram_bytes_per_launch": 123.0}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench._recorded_traffic("long128k") == 123.0
+    assert bench._recorded_traffic("self8k") is None
+    src.write_text("int f() { return 2; }\n")
+    assert bench._recorded_traffic("long128k") is None

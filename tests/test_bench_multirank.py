@@ -55,3 +55,41 @@ def test_reference_arm_only_rank0_prints():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _replica_target(out):
+    import bench
+    rank, world = int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"])
+    assert os.environ["LOCAL_RANK"] == str(rank) and os.environ["MASTER_ADDR"] == "127.0.0.1"
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        out[rank] = (world, bench.max_over_ranks(1.0 + rank, dist))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+    return 0
+
+
+def test_run_replicas_sets_the_rank_environment():
+    # bench.py --gpus N without a launcher starts N ranks itself; each sees the
+    # environment torchrun would set and can rendezvous on 127.0.0.1.
+    sys.path.insert(0, ROOT)
+    import bench
+    out = mp.get_context("spawn").Manager().dict()
+    assert bench.run_replicas(3, _replica_target, (out,)) == 0
+    assert dict(out) == {0: (3, 3.0), 1: (3, 3.0), 2: (3, 3.0)}
+
+
+def test_gpus_flag_without_launcher_starts_the_ranks():
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--workload", "tiny", "--steps", "1", "--warmup", "0",
+                        "--ref-step-seconds", "0.2"], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    import json
+    lines = [x for x in r.stdout.strip().splitlines() if x.startswith("{")]
+    assert len(lines) == 1  # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2

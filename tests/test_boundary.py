@@ -106,6 +106,22 @@ def test_splitkv_workspace_bytes(lib):
     assert 1 <= attn.splitkv_num_splits(1, 1, 100, 4096) <= 8
 
 
+@pytest.mark.parametrize("B,H,Sq,Sk,splits", [
+    (1 << 31, 1 << 21, 1, 384, 3),       # each size below the per-size check, product huge
+    ((1 << 31) - 1, 2, 1, 384, 3),       # more than 2^31 - 1 CTAs
+    (1, (1 << 30), 512, 384, 3),
+    (1 << 40, 1, 1, 384, 2),             # one size beyond 2^31 - 1
+])
+def test_splitkv_workspace_bytes_never_overflows(lib, B, H, Sq, Sk, splits):
+    n = lib.attn_fwd_splitkv_workspace_bytes(B, H, Sq, Sk, 128, splits)
+    assert n == attn.ATTN_ERR_TOO_LARGE
+    # The no-allocation entry point passes the status on (it sizes its scratch
+    # with the same function) and launches nothing; the pointers are never used.
+    st = attn.attn_fwd_splitkv_noalloc_raw(A, 2 * A, 3 * A, 4 * A, 0, B, H, Sq, Sk, 128, 0.088, 0,
+                                           splits, 0)
+    assert st == attn.ATTN_ERR_TOO_LARGE
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(splits=0), attn.ATTN_ERR_INVALID_ARG),
     (dict(splits=9), attn.ATTN_ERR_INVALID_ARG),          # 1000 keys = 8 tiles

@@ -100,3 +100,23 @@ def test_persistent_equals_one_cta_per_item_bitwise():
     torch.cuda.synchronize()
     assert _items(B, H, Sq) > _sms() >= _items(B, step, Sq)
     assert torch.equal(whole.view(torch.int16), torch.cat(parts, dim=1).view(torch.int16))
+
+
+def test_persistent_sign_bit_nans_come_out_canonical():
+    # NaNs with the sign bit set, in V (0xFFC1) and in Q (0xFFFF), on the persistent
+    # path: every NaN output must be the one pattern 0x7FC0 in every mode.
+    layout, B, H, Sq, Sk = "bhsd", 1, 180, 260, 140
+    assert _items(B, H, Sq) > _sms()
+    q, k, v = _qkv(layout, B, H, H, Sq, Sk, seed=1310)
+    q.view(torch.int16)[0, 9, 100, 17] = -1          # 0xFFFF: row 100 of head 9 is NaN
+    v.view(torch.int16)[0, 5, 17, 33] = -63          # 0xFFC1: column 33 of head 5 is NaN
+    exact = attention_fp64(f64_of(q), f64_of(k), f64_of(v), inputs.default_scale(), layout)
+    for mode in inputs.ROUNDINGS:
+        out = attn.attn_fwd(q.cuda(), k.cuda(), v.cuda(), layout=layout, rounding=mode)
+        torch.cuda.synchronize()
+        assert attn.attn_fwd_last_error() == attn.ATTN_OK
+        got = bits_of(out)
+        assert (got[0, 9, 100] == 0x7FC0).all() and (got[0, 5, :, 33] == 0x7FC0).all()
+        stats = compare(got, exact, mode)
+        assert stats["n_nonfinite"] == 128 + Sq - 1
+        assert_parity(stats, excess=True)

@@ -2,16 +2,20 @@
 scratch array, for callers that cannot allocate device memory when they need
 attention (a framework pool that owns all allocations, a serving loop that must
 not call cudaMalloc/cudaFree after start-up). Called through the C ABI and
-compared with attn_fwd_splitkv (caller-provided workspace) on two calls in a
-row, since every call reuses the same scratch. This file is collected last."""
+compared bit for bit with attn_fwd_splitkv (caller-provided workspace, same
+split count) on two calls in a row, since every call reuses the same scratch,
+after another problem has left its own contents there, and against the fp64
+oracle. This file is collected last."""
 import pytest
 import torch
 
 import bf16_forward_attention_gb300 as attn
 from bf16_forward_attention_gb300 import build, inputs
-from oracle import nonfinite_bits, ulp_distance
+import numpy as np
 
-from _parity import ULP_FRACTION, bits_of
+from oracle import attention_fp64
+
+from _parity import assert_parity, bits_of, compare, f64_of
 
 pytestmark = pytest.mark.gpu
 
@@ -45,14 +49,43 @@ def test_noalloc_matches_workspace_entry_point_twice(layout, B, H, Sq, Sk, split
     ref = attn.attn_fwd_splitkv(q, k, v, num_splits=splits, layout=layout)
     torch.cuda.synchronize()
     want = bits_of(ref)
+    # The same kernels with the same split count run in a fixed order, so the
+    # two entry points must agree bit for bit.
     for _ in range(2):  # the second call runs over the first call's scratch contents
         out = torch.full_like(q, float("nan"))
         assert _noalloc(q, k, v, out, layout, splits) == attn.ATTN_OK
         torch.cuda.synchronize()
         assert attn.attn_fwd_last_error() == attn.ATTN_OK
-        got = bits_of(out)
-        assert (nonfinite_bits(got) == nonfinite_bits(want)).all()
-        assert (ulp_distance(got, want) <= 1).mean() >= ULP_FRACTION
+        assert np.array_equal(bits_of(out), want)
+    # And both against the fp64 oracle, element by element.
+    exact = attention_fp64(f64_of(q), f64_of(k), f64_of(v), inputs.default_scale(), layout)
+    assert_parity(compare(want, exact, "rtne"), excess=Sk < 4096)
+
+
+def test_noalloc_scratch_left_by_another_problem():
+    # Problem A, then problem B (other inputs, more splits, more heads: it writes
+    # scratch that A's layout reads) on the same stream, then A again: the stale
+    # contents B left must not leak into A's result.
+    layout = "bhsd"
+    wa = inputs.Workload("noalloc_a", layout, 1, 4, 260, 3000, seed=811)
+    wb = inputs.Workload("noalloc_b", layout, 2, 6, 500, 4100, seed=812)
+    qa, ka, va = (t.cuda() for t in inputs.make_qkv(wa))
+    qb, kb, vb = (t.cuda() for t in inputs.make_qkv(wb))
+    sa, sb = 3, 11
+    assert attn.splitkv_workspace_bytes(2, 6, 500, 4100, sb) > attn.splitkv_workspace_bytes(
+        1, 4, 260, 3000, sa)
+    want_a = bits_of(attn.attn_fwd_splitkv(qa, ka, va, num_splits=sa, layout=layout))
+    want_b = bits_of(attn.attn_fwd_splitkv(qb, kb, vb, num_splits=sb, layout=layout))
+    outs = []
+    for (q, k, v, s) in [(qa, ka, va, sa), (qb, kb, vb, sb), (qa, ka, va, sa)]:
+        out = torch.full_like(q, float("nan"))
+        assert _noalloc(q, k, v, out, layout, s) == attn.ATTN_OK
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert attn.attn_fwd_last_error() == attn.ATTN_OK
+    assert np.array_equal(bits_of(outs[0]), want_a)
+    assert np.array_equal(bits_of(outs[1]), want_b)
+    assert np.array_equal(bits_of(outs[2]), want_a)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
