@@ -74,8 +74,11 @@ int device_ready(int dev) {
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>)};
   for (const void* fn : variants) {
     const bool persist = fn == variants[5];
+    const bool row_limit = fn == variants[2] || fn == variants[3] || fn == variants[4];
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             persist ? attn::kSmemBytesPersist : attn::kSmemBytes) != cudaSuccess) {
+                             persist ? attn::kSmemBytesPersist
+                                     : (row_limit ? attn::kSmemBytesRowLimit : attn::kSmemBytes)) !=
+        cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_LAUNCH;
     }
@@ -269,7 +272,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
   if (causal) {
     attn::attn_fwd_kernel<false, true, false>
-        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+        <<<grid, attn::kThreads, attn::kSmemBytesRowLimit, cs>>>(tq, tk, tv, to, p);
   } else if (n_splits == 1 && p.kv_tiles <= kPersistMaxKvTiles && p.n_items > g_dev_sms[dev]) {
     attn::attn_fwd_kernel<false, false, false, true>
         <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
@@ -401,10 +404,10 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
   const unsigned grid = static_cast<unsigned>(B * Hq * n_qpairs);
   if (p.causal)
     attn::attn_fwd_kernel<false, true, true>
-        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+        <<<grid, attn::kThreads, attn::kSmemBytesRowLimit, cs>>>(tq, tk, tv, to, p);
   else
     attn::attn_fwd_kernel<false, false, true>
-        <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
+        <<<grid, attn::kThreads, attn::kSmemBytesRowLimit, cs>>>(tq, tk, tv, to, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;
 }

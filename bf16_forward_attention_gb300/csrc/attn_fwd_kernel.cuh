@@ -9,7 +9,9 @@
 // 128-key tile of K and V through a 4-stage shared-memory ring. Roles (warps):
 //   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ...
 //   warp 1      TMEM allocator and the single tcgen05.mma issuer
-//   warps 2-3   idle (they complete the first warpgroup)
+//   warps 2-3   causal and variable-length variants: check V of the key tiles
+//               where some row hides keys for NaN / Inf (see "V check" below);
+//               otherwise idle (they complete the first warpgroup)
 //   warps 4-7   softmax + epilogue of query tile 0 (one TMEM lane = one row)
 //   warps 8-11  softmax + epilogue of query tile 1
 // The launch gives every thread 168 registers; the first warpgroup hands most of
@@ -89,7 +91,9 @@ enum : int {
   kBarDrain = kBarOFull + kQTiles,
   kBarQFree = kBarDrain + 1,  // persistent: the Q buffer may be refilled (next item)
   kBarOFree = kBarQFree + 1,  // persistent, per query tile: the epilogue has read O
-  kBarCount = kBarOFree + kQTiles
+  kBarVChk = kBarOFree + kQTiles,  // key-limit variants: V of masked tile m checked (m < 3)
+  kBarVLanded = kBarVChk + 3,      // key-limit variants: V of masked tile m is in the ring
+  kBarCount = kBarVLanded + 3
 };
 
 constexpr int kOffQ = 0;
@@ -100,6 +104,17 @@ constexpr int kOffAbort = kOffTmemSlot + 4;
 constexpr int kSmemUsed = kOffAbort + 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack to align the base to 1024 B
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Variants with a key limit per row (causal, variable-length batch): a record of
+// the non-finite values found in V of each masked key tile (at most 3 per CTA):
+// a flag word, a 128-bit mask of the keys that hold one, and per key three
+// 128-bit column masks (NaN, +Inf, -Inf). 388 words per tile.
+constexpr int kMaxMaskedTiles = 3;
+constexpr int kVRecWords = 4 + 4 + 3 * kBN * 4;
+constexpr int kVRecKeyMask = 4, kVRecNan = 8, kVRecPos = kVRecNan + kBN * 4,
+              kVRecNeg = kVRecPos + kBN * 4;
+constexpr int kOffVRec = (kSmemUsed + 15) & ~15;
+constexpr int kSmemBytesRowLimit = kOffVRec + kMaxMaskedTiles * kVRecWords * 4 + 1024;
+static_assert(kSmemBytesRowLimit <= 232448, "shared memory budget (key-limit variants)");
 // The persistent variant also stages its output: 4 KiB per softmax warp (32
 // rows x 64 columns, one TMA box), so that the Q buffer can be refilled for the
 // next item while the current one is being stored.
@@ -545,6 +560,17 @@ __device__ __forceinline__ Work work_of(const Params& p) {
   return work_of<kCausal, kVarlen>(p, blockIdx.x);
 }
 
+// First key tile of a work item in which some row of the CTA does not see every
+// key (the causal diagonal; the end of a variable-length sequence, where the tile
+// runs into the next sequence's keys), or n_kv if there is none. The masked
+// tiles [first, n_kv) are at most kMaxMaskedTiles: the CTA's 256 rows' key
+// limits span at most 255 keys.
+template <bool kCausal>
+__device__ __forceinline__ int first_masked_tile(const Work& w) {
+  const int min_lim = kCausal ? min(2 * kBM * w.pair + (w.sk - w.sq) + 1, w.sk) : w.sk;
+  return min_lim <= 0 ? 0 : min(min_lim / kBN, w.n_kv);
+}
+
 // kPartial: the CTA covers one split of the key range and writes its fp32 partial
 // result to the workspace (combined by attn_splitkv_combine); otherwise the CTA
 // covers all keys and stores bf16 output. kCausal: the causal mask (p.causal
@@ -614,6 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kBarDrain), 1);
     ptx::mbar_init(bar(kBarQFree), 1);
     for (int t = 0; t < kQTiles; ++t) ptx::mbar_init(bar(kBarOFree + t), 128);
+    for (int m = 0; m < kMaxMaskedTiles; ++m) {
+      ptx::mbar_init(bar(kBarVChk + m), 1);
+      ptx::mbar_init(bar(kBarVLanded + m), 1);
+    }
+    if (kRowLimit)
+      for (int m = 0; m < kMaxMaskedTiles; ++m)
+        reinterpret_cast<uint32_t*>(smem + kOffVRec)[m * kVRecWords] = 0;  // no non-finite V yet
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -804,7 +837,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ktile += n_kv;
           }
         } else {
-          const int n_kv = work_of<kCausal, kVarlen>(p).n_kv;
+          const Work wk = work_of<kCausal, kVarlen>(p);
+          const int n_kv = wk.n_kv;
+          // Masked key tiles (key-limit variants): V is checked first.
+          const int jm = kRowLimit ? first_masked_tile<kCausal>(wk) : n_kv;
           bool ok = wait_bounded(bar(kBarQ), 0, abort_flag, p.timeout_ns, true);
           ptx::tc_fence_after();
           auto ring_wait = [&](int it) -> bool {
@@ -830,11 +866,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(bar(kBarSFull + 1));
             ptx::mma_commit(bar(kBarKvEmpty + 0));
           }
+          // V of a masked key tile: tell the V check it has landed, one key tile
+          // ahead of its P V products.
+          if (kRowLimit && ok && jm == 0 && (ok = ring_wait(1))) ptx::mbar_arrive(bar(kBarVLanded + 0));
           for (int j = 0; ok && j < n_kv; ++j) {
             const int vit = 2 * j + 1;
             const int kit = 2 * j + 2;
             const bool more = j + 1 < n_kv;
             if (!(ok = ring_wait(vit))) break;
+            if (kRowLimit && j >= jm && j - jm < kMaxMaskedTiles &&
+                !(ok = wait_bounded(bar(kBarVChk + (j - jm)), 0, abort_flag, p.timeout_ns, true)))
+              break;
             if (!(ok = wait_bounded(bar(kBarPFull + 0), j & 1, abort_flag, p.timeout_ns, true))) break;
             ptx::tc_fence_after();
             const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
@@ -854,6 +896,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               issue_s(tmem + kTmemS0 + 128, q1_desc, k_desc(kit));
               ptx::mma_commit(bar(kBarSFull + 1));
               ptx::mma_commit(bar(kBarKvEmpty + kit % kStages));
+              const int mnext = j + 1 - jm;  // the next key tile's index among the masked ones
+              if (kRowLimit && mnext >= 0 && mnext < kMaxMaskedTiles) {
+                if (!(ok = ring_wait(vit + 2))) break;
+                ptx::mbar_arrive(bar(kBarVLanded + mnext));
+              }
             }
           }
         }
@@ -863,6 +910,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
       }
       __syncwarp();
+    } else if constexpr (kRowLimit) {
+      // ------------------------------------------------------------ V check (warps 2-3)
+      // In a masked key tile a row's hidden keys get P = 0, and the tensor pipe's
+      // 0 * NaN or 0 * Inf would carry a non-finite V value at such a key into
+      // that row. These two warps read each masked tile's V from the ring before
+      // its first P V product. If it holds non-finite values they record each one
+      // (key, column, kind) and set it to 0 in shared memory; the epilogue then
+      // adds it back to exactly the rows that see its key. Decisions are taken
+      // at barriers of both warps (with a reduction), so neither can leave while
+      // the other waits.
+      const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..63
+      const Work wk = work_of<kCausal, kVarlen>(p);
+      const int jm = first_masked_tile<kCausal>(wk);
+      dbg_ok(wk.n_kv - jm <= kMaxMaskedTiles);
+      for (int m = 0; jm + m < wk.n_kv && m < kMaxMaskedTiles; ++m) {
+        const int fill = 2 * (jm + m) + 1;  // ring fill that holds V of key tile jm + m
+        // The MMA issuer, which follows the ring's phases in order, reports when
+        // this fill has landed (a wait on the ring barrier itself could be more
+        // than one phase ahead of it, which a parity wait cannot tell apart).
+        const bool ok = wait_bounded(bar(kBarVLanded + m), 0, abort_flag, p.timeout_ns, true);
+        if (ptx::named_barrier_or(1, 64, !ok)) break;
+        const uint32_t vt = sRing + (fill % kStages) * kTileBytes;
+        // 2048 chunks of 16 bytes; thread tid reads chunks tid, tid + 64, ...
+        uint32_t acc0 = 0, acc1 = 0;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+          const uint4 x = ptx::ld_shared_v4(vt + (tid + 64 * i) * 16);
+          acc0 = ptx::bf16x2_nonfinite_acc(x.x, ptx::bf16x2_nonfinite_acc(x.y, acc0));
+          acc1 = ptx::bf16x2_nonfinite_acc(x.z, ptx::bf16x2_nonfinite_acc(x.w, acc1));
+        }
+        const bool found = ptx::named_barrier_or(1, 64, (acc0 | acc1) != 0);
+        uint32_t* rec = reinterpret_cast<uint32_t*>(smem + kOffVRec) + m * kVRecWords;
+        if (found) {
+          for (int i = tid; i < kVRecWords; i += 64) rec[i] = 0;
+          ptx::named_barrier_sync(1, 64);
+          for (int i = 0; i < 32; ++i) {
+            const int ci = tid + 64 * i;
+            uint32_t w[4];
+            const uint4 x = ptx::ld_shared_v4(vt + ci * 16);
+            w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+            bool dirty = false;
+            const int key = (ci >> 3) & (kBN - 1);  // TMA box row
+            // 128-byte swizzle: the row's 16-byte chunk c sits at position c ^ (row & 7).
+            const int col0 = (ci >> 10) * 64 + (((ci & 7) ^ (key & 7)) << 3);
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t h = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+              if ((h & 0x7F80u) != 0x7F80u) continue;
+              const int col = col0 + e;
+              const int kind = (h & 0x7Fu) ? kVRecNan : ((h & 0x8000u) ? kVRecNeg : kVRecPos);
+              atomicOr(&rec[kVRecKeyMask + (key >> 5)], 1u << (key & 31));
+              atomicOr(&rec[kind + key * 4 + (col >> 5)], 1u << (col & 31));
+              w[e >> 1] &= ~(0xFFFFu << (16 * (e & 1)));
+              dirty = true;
+            }
+            if (dirty) ptx::st_shared_v4(vt + ci * 16, w[0], w[1], w[2], w[3]);
+          }
+          ptx::fence_proxy_async_smem();  // the zeros, before the tensor pipe reads V
+          ptx::named_barrier_sync(1, 64);
+        }
+        if (tid == 0) {
+          rec[0] = found ? 1u : 0u;
+          ptx::mbar_arrive(bar(kBarVChk + m));
+        }
+      }
     }
   } else {
     ptx::setmaxnreg_inc<kRegsHigh>();
@@ -1183,7 +1294,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage_base = sQ + t * kTileBytes;
         const int mode = p.mode;
         const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
-        const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
+        uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
+        if constexpr (kRowLimit) {
+          // Non-finite V values the check took out of the masked tiles: each key
+          // this row sees adds its value, times a positive weight, to the column
+          // (NaN stays NaN; +Inf and -Inf together give NaN); keys the row does
+          // not see add nothing. Applied after normalisation, so that a row that
+          // is NaN already stays NaN.
+          const int jm = first_masked_tile<kCausal>(wk);
+          const int nm = min(wk.n_kv - jm, kMaxMaskedTiles);
+          const uint32_t* rec0 = reinterpret_cast<const uint32_t*>(smem + kOffVRec);
+          bool any = false;
+          for (int m = 0; m < nm; ++m)
+            if (wait_bounded(bar(kBarVChk + m), 0, abort_flag, p.timeout_ns, true))
+              any |= rec0[m * kVRecWords] != 0;
+          if (any) {
+            // One 32-column word of the three masks at a time (few live registers
+            // next to the 128-column row).
+            const float pos_inf = __int_as_float(0x7F800000);
+#pragma unroll
+            for (int cw = 0; cw < 4; ++cw) {
+              uint32_t pn = 0, pp = 0, pm = 0;
+              for (int m = 0; m < nm; ++m) {
+                const uint32_t* rec = rec0 + m * kVRecWords;
+                if (!rec[0]) continue;
+                const int vis = row_lim - kBN * (jm + m);  // keys of this tile the row sees
+                for (int wd = 0; wd < 4; ++wd) {
+                  const int lim = vis - 32 * wd;
+                  uint32_t km = lim <= 0 ? 0u : rec[kVRecKeyMask + wd];
+                  if (lim < 32) km &= (1u << (lim > 0 ? lim : 0)) - 1u;
+                  while (km) {
+                    const int key = 32 * wd + __ffs(km) - 1;
+                    km &= km - 1;
+                    pn |= rec[kVRecNan + key * 4 + cw];
+                    pp |= rec[kVRecPos + key * 4 + cw];
+                    pm |= rec[kVRecNeg + key * 4 + cw];
+                  }
+                }
+              }
+              auto special = [&](int b) -> float {
+                if (((pn | (pp & pm)) >> b) & 1u) return __int_as_float(0x7FC00000);
+                if ((pp >> b) & 1u) return pos_inf;
+                if ((pm >> b) & 1u) return -pos_inf;
+                return -0.0f;  // x + (-0) = x for every x, signed zeros included
+              };
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                acc[16 * cw + i] = ptx::f2_add(ptx::f2_mul(acc[16 * cw + i], inv2),
+                                               ptx::f2_pack(special(2 * i), special(2 * i + 1)));
+            }
+            inv2 = ptx::f2_pack(1.0f, 1.0f);
+          }
+        }
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t w[16];

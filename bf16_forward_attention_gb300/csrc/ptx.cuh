@@ -410,5 +410,42 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// acc + a * 0 on two bf16 lanes: a finite a leaves acc unchanged (acc starts at
+// +0 and +0 + -0 = +0), an infinite or NaN a makes it NaN, and NaN stays NaN.
+__device__ __forceinline__ uint32_t bf16x2_nonfinite_acc(uint32_t a, uint32_t acc) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(0u), "r"(acc));
+  return d;
+}
+
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id`
+// (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// The same barrier, returning the OR of `pred` over the participating threads.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 }  // namespace ptx
 }  // namespace attn

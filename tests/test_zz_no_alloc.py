@@ -68,12 +68,12 @@ def test_noalloc_scratch_left_by_another_problem():
     # contents B left must not leak into A's result.
     layout = "bhsd"
     wa = inputs.Workload("noalloc_a", layout, 1, 4, 260, 3000, seed=811)
-    wb = inputs.Workload("noalloc_b", layout, 2, 6, 500, 4100, seed=812)
+    wb = inputs.Workload("noalloc_b", layout, 1, 6, 500, 4100, seed=812)
     qa, ka, va = (t.cuda() for t in inputs.make_qkv(wa))
     qb, kb, vb = (t.cuda() for t in inputs.make_qkv(wb))
     sa, sb = 3, 11
-    assert attn.splitkv_workspace_bytes(2, 6, 500, 4100, sb) > attn.splitkv_workspace_bytes(
-        1, 4, 260, 3000, sa)
+    need_b = attn.splitkv_workspace_bytes(1, 6, 500, 4100, sb)
+    assert attn.splitkv_workspace_bytes(1, 4, 260, 3000, sa) < need_b <= 32 << 20
     want_a = bits_of(attn.attn_fwd_splitkv(qa, ka, va, num_splits=sa, layout=layout))
     want_b = bits_of(attn.attn_fwd_splitkv(qb, kb, vb, num_splits=sb, layout=layout))
     outs = []
