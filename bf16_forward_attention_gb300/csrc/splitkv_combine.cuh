@@ -24,9 +24,8 @@ struct CombineParams {
 };
 
 // Four query rows per block of 128 threads: 32 threads per row, each owning four
-// consecutive output columns (16-byte loads of the partial rows). The loops over
-// the splits are unrolled so that their independent loads overlap; the sums still
-// run in split order.
+// consecutive output columns (16-byte loads of the partial rows); the merge
+// itself is merge_splits4, shared with the split kernel's own merge.
 constexpr int kCombineRows = 4;
 
 __global__ void __launch_bounds__(kD) attn_splitkv_combine(const CombineParams p) {
@@ -34,38 +33,13 @@ __global__ void __launch_bounds__(kD) attn_splitkv_combine(const CombineParams p
   if (q >= p.Sq) return;
   const int bh = blockIdx.y;
   const int c0 = (threadIdx.x & 31) * 4;
-  const float2* rl = reinterpret_cast<const float2*>(p.part_rl);
   const size_t split_pitch = static_cast<size_t>(p.BH) * p.sq_pad;
-  const size_t row0 = static_cast<size_t>(bh) * p.sq_pad + q;
-
-  // R = max over splits of r_s. A split with no finite logit has r_s = -Inf and
-  // weight 0 (its sums are 0, or NaN which then propagates as it must). If every
-  // split is like that, R = 0 keeps the weights at 0 and 0/0 gives NaN.
-  float R = -__int_as_float(0x7F800000);
-#pragma unroll 8
-  for (int s = 0; s < p.n_splits; ++s) R = fmaxf(R, rl[row0 + s * split_pitch].x);
-  if (R == -__int_as_float(0x7F800000)) R = 0.f;
-  float L = 0.f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = 0; s < p.n_splits; ++s) {
-    const size_t r = row0 + s * split_pitch;
-    const float2 ml = rl[r];
-    const float w = ptx::ex2(ml.x - R);  // NaN only if R = +Inf: that row is NaN anyway
-    const float4 x = *reinterpret_cast<const float4*>(p.part_o + r * kD + c0);
-    L = fmaf(ml.y, w, L);
-    o.x = fmaf(x.x, w, o.x);
-    o.y = fmaf(x.y, w, o.y);
-    o.z = fmaf(x.z, w, o.z);
-    o.w = fmaf(x.w, w, o.w);
-  }
-  const float inv = __frcp_rn(L);
+  const uint2 o = merge_splits4(p.part_o, p.part_rl, static_cast<size_t>(bh) * p.sq_pad + q,
+                                split_pitch, p.n_splits, c0, p.mode);
   const int b = bh / p.H, h = bh % p.H;
   const size_t idx = p.layout == 0 ? ((static_cast<size_t>(b) * p.H + h) * p.Sq + q) * kD + c0
                                    : ((static_cast<size_t>(b) * p.Sq + q) * p.H + h) * kD + c0;
-  const uint32_t lo = round_bf16_bits(o.x * inv, p.mode) | (round_bf16_bits(o.y * inv, p.mode) << 16);
-  const uint32_t hi = round_bf16_bits(o.z * inv, p.mode) | (round_bf16_bits(o.w * inv, p.mode) << 16);
-  *reinterpret_cast<uint2*>(p.out + idx) = make_uint2(lo, hi);
+  *reinterpret_cast<uint2*>(p.out + idx) = o;
 }
 
 }  // namespace attn
