@@ -294,10 +294,23 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
     cp.sq_pad = p.sq_pad;
     cp.layout = layout;
     cp.mode = rounding_mode;
-    attn::attn_splitkv_combine<<<dim3(static_cast<unsigned>((Sq + attn::kCombineRows - 1) /
-                                                            attn::kCombineRows),
-                                      static_cast<unsigned>(B * H)),
-                                 attn::kD, 0, cs>>>(cp);
+    // Programmatic dependent launch: the merge grid is set up while the split
+    // kernel runs and waits on the device for its completion.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((Sq + attn::kCombineRows - 1) / attn::kCombineRows),
+                       static_cast<unsigned>(B * H));
+    cfg.blockDim = dim3(attn::kD);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn::attn_splitkv_combine, cp) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_LAUNCH;
   return ATTN_OK;

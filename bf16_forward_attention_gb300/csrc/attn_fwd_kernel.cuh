@@ -686,6 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
+  // The split variant's merge kernel may be scheduled as soon as every CTA of
+  // this grid has started (it waits for the whole grid before reading).
+  if constexpr (kPartial) ptx::launch_dependents();
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tm_q);
     ptx::prefetch_tmap(&tm_k);

@@ -427,6 +427,18 @@ __device__ __forceinline__ uint32_t bf16x2_nonfinite_acc(uint32_t a, uint32_t ac
   return d;
 }
 
+// Programmatic dependent launch: the next kernel on the stream (launched with
+// programmatic stream serialisation) may be scheduled once every CTA of this
+// grid has executed launch_dependents or exited; it then waits with
+// grid_dependency_wait until this grid has completed and its writes are visible.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Barrier among `count` threads (a multiple of 32) on hardware barrier `id`
 // (1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {

@@ -28,7 +28,10 @@ struct CombineParams {
 // itself is merge_splits4, shared with the split kernel's own merge.
 constexpr int kCombineRows = 4;
 
+// Launched as a programmatic dependent of the split kernel: it may start while
+// the split kernel's last CTAs still run, and waits here for that grid's writes.
 __global__ void __launch_bounds__(kD) attn_splitkv_combine(const CombineParams p) {
+  ptx::grid_dependency_wait();
   const int q = blockIdx.x * kCombineRows + (threadIdx.x >> 5);
   if (q >= p.Sq) return;
   const int bh = blockIdx.y;
