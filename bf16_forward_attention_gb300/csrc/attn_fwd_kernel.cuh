@@ -710,6 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::setmaxnreg_dec<kRegsLow>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
+      // L2 policies: query tiles are read once, key/value tiles by every CTA of
+      // their head.
+      const uint64_t pol_once = ptx::l2_policy_evict_first();
+      const uint64_t pol_reuse = ptx::l2_policy_evict_last();
       if constexpr (kPersist) {
         if (lane == 0) {
           int issued = 0;   // ring fills started so far (fill i goes to stage i % kStages)
@@ -726,8 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < kQTiles; ++t) {
               tma_coords(p.layout, wk.q_base + (2 * wk.pair + t) * kBM, wk.head, c1, c2);
               for (int hf = 0; hf < 2; ++hf)
-                ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1,
-                                 c2, wk.batch);
+                ptx::tma_load_4d_hint(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf,
+                                      c1, c2, wk.batch, pol_once);
             }
             ++q_loads;
             planned += 2 * wk.n_kv;
@@ -742,8 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_coords(p.layout, wk.k_base + (wk.tile0 + (it >> 1)) * kBN, wk.kv_head, c1, c2);
               ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
               for (int hf = 0; hf < 2; ++hf)
-                ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map,
-                                 bar(kBarKvFull + stage), 64 * hf, c1, c2, wk.batch);
+                ptx::tma_load_4d_hint(sRing + stage * kTileBytes + hf * kHalfBytes, map,
+                                      bar(kBarKvFull + stage), 64 * hf, c1, c2, wk.batch, pol_reuse);
               ++issued;
             }
             if (!ok) break;
@@ -771,8 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < kQTiles; ++t) {
             tma_coords(p.layout, q_base + (2 * pair + t) * kBM, head, c1, c2);
             for (int hf = 0; hf < 2; ++hf)
-              ptx::tma_load_4d(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1, c2,
-                               batch);
+              ptx::tma_load_4d_hint(sQ + t * kTileBytes + hf * kHalfBytes, &tm_q, bar(kBarQ), 64 * hf, c1,
+                                    c2, batch, pol_once);
           }
           for (int it = 0; it < 2 * n_kv; ++it) {
             const int stage = it % kStages;
@@ -783,8 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_coords(p.layout, k_base + (tile0 + (it >> 1)) * kBN, kv_head, c1, c2);
             ptx::mbar_arrive_expect_tx(bar(kBarKvFull + stage), kTileBytes);
             for (int hf = 0; hf < 2; ++hf)
-              ptx::tma_load_4d(sRing + stage * kTileBytes + hf * kHalfBytes, map, bar(kBarKvFull + stage),
-                               64 * hf, c1, c2, batch);
+              ptx::tma_load_4d_hint(sRing + stage * kTileBytes + hf * kHalfBytes, map,
+                                    bar(kBarKvFull + stage), 64 * hf, c1, c2, batch, pol_reuse);
             ++issued;
           }
           // Let every copy this thread started land before the CTA can exit. On
@@ -1177,7 +1181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && q_row0 < p.Sq && dbg_ok(q_row0 >= 0)) {
             int c1, c2;
             tma_coords(p.layout, q_row0, wk.head, c1, c2);
-            ptx::tma_store_4d(&tm_o, stage_w, 64 * hf, c1, c2, wk.batch);
+            ptx::tma_store_4d_hint(&tm_o, stage_w, 64 * hf, c1, c2, wk.batch,
+                                   ptx::l2_policy_evict_first());
             ptx::bulk_commit_group();
           }
         }
@@ -1410,8 +1415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int c1, c2;
             tma_coords(p.layout, wk.q_base + q_row0, wk.head, c1, c2);
             for (int hf = 0; hf < 2; ++hf)
-              ptx::tma_store_4d(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1, c2,
-                                wk.batch);
+              ptx::tma_store_4d_hint(&tm_o, stage_base + hf * kHalfBytes + wq * 32 * 128, 64 * hf, c1,
+                                     c2, wk.batch, ptx::l2_policy_evict_first());
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_0();
           }
