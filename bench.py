@@ -155,6 +155,14 @@ def run_replicas(world: int, target, target_args=()) -> int:
              for r in range(world)]
     for pr in procs:
         pr.start()
+    # A rank that fails would leave the others waiting at a barrier: end them.
+    while any(pr.is_alive() for pr in procs):
+        if any(pr.exitcode not in (None, 0) for pr in procs):
+            for pr in procs:
+                if pr.is_alive():
+                    pr.terminate()
+            break
+        time.sleep(0.2)
     for pr in procs:
         pr.join()
     return 0 if all(pr.exitcode == 0 for pr in procs) else 1

@@ -104,7 +104,10 @@ enum { ATTN_FLAG_CAUSAL = 1 };
  *            j <= i + (Sk - Sq) (aligned at the bottom right, so the last query
  *            sees every key); hidden logits are -Inf, and a query that sees no
  *            key (possible when Sq > Sk) comes out NaN. Key tiles that no row of
- *            a query tile can see are skipped.
+ *            a query tile can see are skipped. A hidden key takes no part at
+ *            all: a NaN or infinity in V at a key a query does not see does not
+ *            reach that query's output, while a query that sees it gets NaN or
+ *            that infinity in the column.
  * Other arguments, ownership, errors and the numerics contract as attn_fwd.
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
@@ -150,7 +153,9 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, int
  *   cu_seqlens_q, cu_seqlens_k
  *        device, int32, B + 1 entries each: sequence b owns query tokens
  *        cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens cu_seqlens_k[b] ..
- *        cu_seqlens_k[b+1]-1, and attends only within itself. Offsets start at
+ *        cu_seqlens_k[b+1]-1, and attends only within itself (another
+ *        sequence's keys take no part, NaN or infinite values in its V
+ *        included). Offsets start at
  *        0, do not decrease and end at total_q / total_k; a sequence may have no
  *        queries (nothing to do) or no keys (its rows come out NaN).
  *   B             number of sequences, >= 1

@@ -93,3 +93,21 @@ def test_gpus_flag_without_launcher_starts_the_ranks():
     assert len(lines) == 1  # rank 0 alone prints
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+def _failing_target(out):
+    rank = int(os.environ["RANK"])
+    if rank == 1:
+        raise SystemExit(3)
+    dist.init_process_group("gloo", rank=rank, world_size=int(os.environ["WORLD_SIZE"]))
+    dist.barrier()  # never completes: rank 1 is gone
+    return 0
+
+
+def test_run_replicas_ends_the_ranks_when_one_fails():
+    sys.path.insert(0, ROOT)
+    import bench
+    import time
+    t0 = time.time()
+    assert bench.run_replicas(2, _failing_target, (None,)) == 1
+    assert time.time() - t0 < 120
