@@ -486,11 +486,13 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
         raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(q.device):
-        stream = torch.cuda.current_stream(q.device).cuda_stream
-        st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                          LAYOUTS[layout], B, H, Sq, Sk, D, float(scale), ROUNDINGS[rounding],
-                          stream)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), LAYOUTS[layout], B, H, Sq, Sk,
+            D, float(scale), ROUNDINGS[rounding])
+    if torch.cuda.current_device() == q.device.index:
+        st = attn_fwd_raw(*args, torch.cuda.current_stream(q.device).cuda_stream)
+    else:
+        with torch.cuda.device(q.device):
+            st = attn_fwd_raw(*args, torch.cuda.current_stream(q.device).cuda_stream)
     if st != ATTN_OK:
         raise AttnError(st, status_str(st))
     return out

@@ -251,3 +251,4 @@ def test_inf_in_v_positions():
     fin_stats = compare(np.where(finite, got, 0).astype(np.uint16), np.where(finite, exact, 0.0),
                         "rtne")
     assert_parity(fin_stats)
+
