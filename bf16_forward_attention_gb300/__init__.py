@@ -200,7 +200,7 @@ def attn_fwd_splitkv(q, k, v, *, num_splits: int | None = None, layout: str = "b
     _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = attn_fwd_splitkv_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                   LAYOUTS[layout], B, H, Sq, Sk, D, float(scale),
@@ -243,7 +243,7 @@ def attn_fwd_ex(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = attn_fwd_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                              LAYOUTS[layout], B, Hq, Hkv, Sq, Sk, D, float(scale),
@@ -299,7 +299,7 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, *,
     _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = attn_fwd_varlen_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                  cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
@@ -361,7 +361,7 @@ def attn_fwd_host(q, k, v, *, causal: bool = False, layout: str = "bhsd",
     _check_out(out, q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(device):
+    with _on_device(device):
         stream = torch.cuda.current_stream(device).cuda_stream
         st = attn_fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                LAYOUTS[layout], B, Hq, Hkv, Sq, Sk, D, float(scale),
@@ -413,7 +413,7 @@ def attn_fwd_varlen_host(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool = 
         out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(device):
+    with _on_device(device):
         stream = torch.cuda.current_stream(device).cuda_stream
         st = load_library().attn_fwd_varlen_host(
             q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), cu_seqlens_q.data_ptr(),
@@ -427,6 +427,19 @@ def attn_fwd_varlen_host(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal: bool = 
 
 def attn_fwd_last_error() -> int:
     return load_library().attn_fwd_last_error()
+
+
+def _on_device(device):
+    """The device context for a library call: none when `device` is already the
+    current CUDA device (entering torch.cuda.device costs a few microseconds, a
+    noticeable share of a small call)."""
+    import contextlib
+
+    import torch
+
+    if torch.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _dims(x, layout):
@@ -486,13 +499,11 @@ def attn_fwd(q, k, v, *, layout: str = "bhsd", scale: float | None = None,
         raise ValueError("out must be a contiguous bf16 tensor shaped like q on q's device")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), LAYOUTS[layout], B, H, Sq, Sk,
-            D, float(scale), ROUNDINGS[rounding])
-    if torch.cuda.current_device() == q.device.index:
-        st = attn_fwd_raw(*args, torch.cuda.current_stream(q.device).cuda_stream)
-    else:
-        with torch.cuda.device(q.device):
-            st = attn_fwd_raw(*args, torch.cuda.current_stream(q.device).cuda_stream)
+    with _on_device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          LAYOUTS[layout], B, H, Sq, Sk, D, float(scale), ROUNDINGS[rounding],
+                          stream)
     if st != ATTN_OK:
         raise AttnError(st, status_str(st))
     return out
