@@ -391,3 +391,30 @@ def test_causal_hidden_keys_take_no_part_even_with_nonfinite_v():
         np.testing.assert_allclose(got[0, 0, i], want, rtol=1e-13, atol=1e-15)
     assert np.isnan(got[0, 0, 4:, 7]).all()
     assert got[0, 0, 5, 9] == np.inf and np.isfinite(got[0, 0, 4, 9])
+
+
+def test_varlen_other_sequences_nonfinite_v_takes_no_part():
+    # Each sequence attends only within itself: NaN and infinities in another
+    # sequence's V leave its rows exactly as if that sequence were alone, and a
+    # sequence's own visible non-finite V shows in its rows.
+    cq, ck = [0, 3, 7], [0, 5, 9]
+    q, k, v = _rand((7, 2, 128), 90), _rand((9, 2, 128), 91), _rand((9, 2, 128), 92)
+    v_bad = v.copy()
+    v_bad[6, 0, 3] = np.nan        # sequence 1, key 1, head 0
+    v_bad[8, 1, 4] = -np.inf       # sequence 1, key 3, head 1
+    v_bad[0, 0, 5] = np.inf        # sequence 0, key 0, head 0
+    for causal in (False, True):
+        got = oracle.attention_varlen_fp64(q, k, v_bad, cq, ck, 0.1, causal=causal)
+        for b in range(2):
+            for h in range(2):
+                sq = cq[b + 1] - cq[b]
+                want = oracle.attention_rows_fp64(q[cq[b]:cq[b + 1], h], k[ck[b]:ck[b + 1], h],
+                                                  v_bad[ck[b]:ck[b + 1], h], 0.1, np.arange(sq),
+                                                  causal=causal)
+                np.testing.assert_allclose(got[cq[b]:cq[b + 1], h], want, rtol=1e-13, atol=1e-15)
+        # Sequence 0 holds none of sequence 1's values; sequence 1 none of sequence 0's.
+        assert np.isfinite(got[0:3, 0, 3]).all() and np.isfinite(got[0:3, 1, 4]).all()
+        assert np.isfinite(got[3:7, 0, 5]).all()
+    got = oracle.attention_varlen_fp64(q, k, v_bad, cq, ck, 0.1)
+    assert np.isnan(got[3:7, 0, 3]).all() and (got[3:7, 1, 4] == -np.inf).all()
+    assert (got[0:3, 0, 5] == np.inf).all()
