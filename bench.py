@@ -404,6 +404,16 @@ def run_ours(args, w):
         splits = attn.splitkv_num_splits(w.B, w.H, w.Sq, w.Sk)
         workspace = torch.empty(max(16, attn.splitkv_workspace_bytes(w.B, w.H, w.Sq, w.Sk, splits)),
                                 dtype=torch.uint8, device=dev)
+    launches_per_call = 2 if splits > 1 else 1
+    split_tail = args.split_tail and splits == 1 and not w.causal and not w.seqlens
+    if split_tail:
+        # The full waves and the pairs are separate launches (one of them when
+        # the call is a single partial wave of pairs, or has no pairs).
+        pairs = attn.split_tail_items(w.B, w.H, w.Sq, w.Sk)
+        if pairs < 0:
+            raise attn.AttnError(pairs, attn.status_str(pairs))
+        n_items = w.B * w.H * -(-w.Sq // 256)
+        launches_per_call = 2 if 0 < pairs < n_items else 1
 
     cu_dev = None
     if w.seqlens:
@@ -418,9 +428,9 @@ def run_ours(args, w):
         if splits > 1:
             return attn.attn_fwd_splitkv(qq, kk, vv, num_splits=splits, layout=w.layout,
                                          rounding=m, out=out, workspace=workspace)
-        if w.causal or w.kv_heads != w.H:
+        if w.causal or w.kv_heads != w.H or split_tail:
             return attn.attn_fwd_ex(qq, kk, vv, causal=w.causal, layout=w.layout, rounding=m,
-                                    out=out)
+                                    out=out, split_tail=split_tail)
         return attn.attn_fwd(qq, kk, vv, layout=w.layout, rounding=m, out=out)
 
     def step():
@@ -601,8 +611,9 @@ def run_ours(args, w):
                               "ridge of the dense bf16 peak over HBM bandwidth")},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": n_calls * (2 if splits > 1 else 1),
+        "gpu_launches": n_calls * launches_per_call,
         "splits": splits,
+        "split_tail": split_tail,
         "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
         "env": _env_record(dev),
@@ -628,6 +639,9 @@ def main(argv=None):
     ap.add_argument("--dist-launches", type=int, default=100,
                     help="launches timed one by one, after the timed steps, for the launch-time "
                          "distribution (at least the timed launches are used if more)")
+    ap.add_argument("--split-tail", action="store_true",
+                    help="run the device calls with ATTN_FLAG_SPLIT_TAIL (the last, partial wave "
+                         "on pairs of CTAs; an item's bits then depend on the size of the call)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the kernel, from an ncu capture")
     args = ap.parse_args(argv)

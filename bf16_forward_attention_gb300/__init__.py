@@ -31,6 +31,7 @@ ATTN_ERR_SCRATCH = -10
 ATTN_ERR_SEQLENS = -11
 ATTN_ERR_DEBUG_CHECK = -12
 ATTN_FLAG_CAUSAL = 1
+ATTN_FLAG_SPLIT_TAIL = 2
 
 _libs: dict = {}
 
@@ -67,7 +68,7 @@ def load_library(debug: bool | None = None) -> ctypes.CDLL:
     lib.attn_fwd_last_error.restype = ctypes.c_int
     lib.attn_fwd_version.argtypes = []
     lib.attn_fwd_version.restype = ctypes.c_int
-    lib.attn_fwd_timeout_selftest.argtypes = lib.attn_fwd.argtypes + [ctypes.c_uint64]
+    lib.attn_fwd_timeout_selftest.argtypes = lib.attn_fwd.argtypes + [ctypes.c_uint64, ctypes.c_int]
     lib.attn_fwd_timeout_selftest.restype = ctypes.c_int
     lib.attn_fwd_splitkv.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64, i64, i64,
                                                              ctypes.c_float, ctypes.c_int,
@@ -76,6 +77,8 @@ def load_library(debug: bool | None = None) -> ctypes.CDLL:
     lib.attn_fwd_splitkv.restype = ctypes.c_int
     lib.attn_fwd_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int]
     lib.attn_fwd_splitkv_workspace_bytes.restype = i64
+    lib.attn_fwd_split_tail_items.argtypes = [i64, i64, i64, i64]
+    lib.attn_fwd_split_tail_items.restype = ctypes.c_int
     lib.attn_fwd_splitkv_num_splits.argtypes = [i64, i64, i64, i64]
     lib.attn_fwd_splitkv_num_splits.restype = ctypes.c_int
     lib.attn_fwd_splitkv_noalloc.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, i64, i64, i64,
@@ -123,12 +126,13 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, 
 
 def attn_fwd_timeout_selftest_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int,
                                   B: int, H: int, Sq: int, Sk: int, d: int, scale: float,
-                                  rounding_mode: int, stream: int, timeout_ns: int) -> int:
+                                  rounding_mode: int, stream: int, timeout_ns: int,
+                                  flags: int = 0) -> int:
     """Direct call of ``attn_fwd_timeout_selftest`` (a launch whose device-side
     wait must time out; see include/attn_fwd.h)."""
     return load_library().attn_fwd_timeout_selftest(q_ptr, k_ptr, v_ptr, out_ptr, layout, B, H, Sq,
                                                     Sk, d, ctypes.c_float(scale), rounding_mode,
-                                                    stream, timeout_ns)
+                                                    stream, timeout_ns, flags)
 
 
 def attn_fwd_splitkv_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, B: int,
@@ -211,6 +215,13 @@ def attn_fwd_splitkv(q, k, v, *, num_splits: int | None = None, layout: str = "b
     return out
 
 
+def split_tail_items(B: int, Hq: int, Sq: int, Sk: int) -> int:
+    """Items of an ``attn_fwd_ex(..., split_tail=True)`` call of this size that run on
+    pairs of CTAs on the current device (0: the flag changes nothing), or a negative
+    status (see include/attn_fwd.h)."""
+    return load_library().attn_fwd_split_tail_items(B, Hq, Sq, Sk)
+
+
 def attn_fwd_ex_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: int, B: int, Hq: int,
                     Hkv: int, Sq: int, Sk: int, d: int, scale: float, rounding_mode: int,
                     flags: int, stream: int) -> int:
@@ -220,9 +231,15 @@ def attn_fwd_ex_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, layout: in
 
 
 def attn_fwd_ex(q, k, v, *, causal: bool = False, layout: str = "bhsd",
-                scale: float | None = None, rounding: str = "rtne", out=None):
+                scale: float | None = None, rounding: str = "rtne", out=None,
+                split_tail: bool = False):
     """attn_fwd with grouped-query heads (k, v may have fewer heads than q, a divisor
-    of q's) and an optional causal mask aligned at the bottom right."""
+    of q's) and an optional causal mask aligned at the bottom right.
+
+    ``split_tail``: run the items of the last, partial wave on pairs of CTAs, each
+    taking half of the key range (ATTN_FLAG_SPLIT_TAIL; no effect with the mask).
+    Faster when that wave is short, but an item's bits then depend on the size
+    of the call."""
     import torch
 
     if layout not in LAYOUTS or rounding not in ROUNDINGS:
@@ -247,7 +264,9 @@ def attn_fwd_ex(q, k, v, *, causal: bool = False, layout: str = "bhsd",
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = attn_fwd_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                              LAYOUTS[layout], B, Hq, Hkv, Sq, Sk, D, float(scale),
-                             ROUNDINGS[rounding], ATTN_FLAG_CAUSAL if causal else 0, stream)
+                             ROUNDINGS[rounding],
+                             (ATTN_FLAG_CAUSAL if causal else 0)
+                             | (ATTN_FLAG_SPLIT_TAIL if split_tail else 0), stream)
     if st != ATTN_OK:
         raise AttnError(st, status_str(st))
     return out
@@ -514,4 +533,5 @@ __all__ = ["attn_fwd", "attn_fwd_raw", "attn_fwd_last_error", "attn_fwd_timeout_
            "splitkv_num_splits", "attn_fwd_splitkv_noalloc_raw", "attn_fwd_ex", "attn_fwd_ex_raw",
            "attn_fwd_varlen", "attn_fwd_varlen_raw", "ATTN_ERR_SEQLENS",
            "attn_fwd_host", "attn_fwd_host_raw", "host_workspace_bytes", "attn_fwd_varlen_host", "status_str", "load_library",
-           "AttnError", "LAYOUTS", "ROUNDINGS", "lib_path", "ATTN_ERR_DEBUG_CHECK"]
+           "AttnError", "LAYOUTS", "ROUNDINGS", "lib_path", "ATTN_ERR_DEBUG_CHECK",
+           "ATTN_FLAG_CAUSAL", "ATTN_FLAG_SPLIT_TAIL", "split_tail_items"]

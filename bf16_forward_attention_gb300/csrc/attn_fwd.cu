@@ -41,12 +41,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 = not set up, 1 = ready, negative = status to return
 int g_dev_sms[kMaxDevices];    // streaming multiprocessors of each device (once ready)
+int g_dev_pairs[kMaxDevices];  // 2-CTA clusters of the pair variant that fit at once
 
 // Whole-range problems with at most this many key tiles run on the persistent
 // variant (one CTA per SM looping over the items) when they have more items
 // than SMs: their items are short, and one CTA per item leaves each SM idle
 // through every item's first loads and final store.
 constexpr int64_t kPersistMaxKvTiles = 16;
+
+// Whole-range problems with at least this many key tiles run the items of their
+// last, partial wave on the pair variant (each item's keys split between the two
+// CTAs of a cluster), when those items fit on the GPU at once as clusters: the
+// wave then takes about half an item's time instead of a whole one.
+constexpr int64_t kPairMinKvTiles = 8;
 
 // Once per device: check the architecture and raise the shared-memory limit.
 int device_ready(int dev) {
@@ -71,12 +78,15 @@ int device_ready(int dev) {
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>),
-      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>)};
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, false, true>)};
   for (const void* fn : variants) {
     const bool persist = fn == variants[5];
+    const bool pair = fn == variants[6];
     const bool row_limit = fn == variants[2] || fn == variants[3] || fn == variants[4];
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              persist ? attn::kSmemBytesPersist
+                             : pair  ? attn::kSmemBytesPair
                                      : (row_limit ? attn::kSmemBytesRowLimit : attn::kSmemBytes)) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -104,8 +114,40 @@ int device_ready(int dev) {
     return ATTN_ERR_NO_DEVICE;
   }
   g_dev_sms[dev] = sms;
+  // How many 2-CTA clusters of the pair variant the device holds at once (SMs
+  // are paired within their GPC, so this can be below half the SM count). If the
+  // query fails the pair variant is not used.
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(sms));
+    cfg.blockDim = dim3(attn::kThreads);
+    cfg.dynamicSmemBytes = attn::kSmemBytesPair;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, variants[6], &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      clusters = 0;
+    }
+    g_dev_pairs[dev] = clusters;
+  }
   g_dev_state[dev] = 1;
   return ATTN_OK;
+}
+
+// Under ATTN_FLAG_SPLIT_TAIL: how many items (those of the last, partial wave of a
+// one-CTA-per-item launch) run on pairs; 0 if none. Problems that take the
+// persistent variant keep it.
+int64_t pair_tail_items(int dev, int64_t n_items, int64_t kv_tiles) {
+  const int64_t sms = g_dev_sms[dev];
+  if (kv_tiles <= kPersistMaxKvTiles && n_items > sms) return 0;
+  const int64_t tail = n_items % sms;
+  return (tail > 0 && tail <= g_dev_pairs[dev] && kv_tiles >= kPairMinKvTiles) ? tail : 0;
 }
 
 // 4-D map over a (B, H, S, 128) bf16 tensor in the given layout, box of
@@ -191,7 +233,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
                   int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale, int rounding_mode,
                   void* stream, unsigned long long timeout_ns, int withhold_s0, int n_splits,
                   void* workspace, int64_t workspace_bytes, int64_t Hkv = 0, int causal = 0,
-                  int dbg_poison = 0) {
+                  int dbg_poison = 0, int split_tail = 0) {
   if (Hkv == 0) Hkv = H;
   // ---- host-side validation (nothing is launched on failure)
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
@@ -267,8 +309,14 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
   p.head_group = head_group_of(B * H, Sk);
   p.dbg_poison = dbg_poison;
   p.n_items = static_cast<int>(B * H * n_qpairs * n_splits);
+  p.item_base = 0;
+  p.early_dependents = 0;
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int64_t n_items1 = B * H * n_qpairs;
+  const int64_t n_tail =
+      (split_tail && !causal && n_splits == 1 && !dbg_poison) ? pair_tail_items(dev, n_items1, p.kv_tiles)
+                                                              : 0;
   const unsigned grid = static_cast<unsigned>(B * H * n_qpairs * n_splits);
   if (causal) {
     attn::attn_fwd_kernel<false, true, false>
@@ -277,6 +325,40 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
     attn::attn_fwd_kernel<false, false, false, true>
         <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
             tq, tk, tv, to, p);
+  } else if (n_tail > 0) {
+    // The full waves as usual, then the tail items as 2-CTA clusters, each with
+    // its key range split in two halves and merged on chip (pair variant).
+    const int64_t n_full = n_items1 - n_tail;
+    if (n_full > 0) {
+      attn::Params pf = p;
+      pf.early_dependents = 1;
+      attn::attn_fwd_kernel<false, false, false>
+          <<<static_cast<unsigned>(n_full), attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, pf);
+    }
+    attn::Params pp = p;
+    pp.n_splits = 2;
+    pp.item_base = static_cast<int>(2 * n_full);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * n_tail));
+    cfg.blockDim = dim3(attn::kThreads);
+    cfg.dynamicSmemBytes = attn::kSmemBytesPair;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // A programmatic dependent of the full waves: its clusters take SMs as the
+    // last full wave drains instead of after the whole launch.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = n_full > 0 ? 2 : 1;
+    if (cudaLaunchKernelEx(&cfg, attn::attn_fwd_kernel<false, false, false, false, true>, tq, tk,
+                           tv, to, pp) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_LAUNCH;
+    }
   } else if (n_splits == 1) {
     attn::attn_fwd_kernel<false, false, false>
         <<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tq, tk, tv, to, p);
@@ -330,10 +412,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
                 int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t d, float scale,
                 int rounding_mode, int flags, void* stream) {
-  if (flags & ~ATTN_FLAG_CAUSAL) return ATTN_ERR_UNSUPPORTED;
+  if (flags & ~(ATTN_FLAG_CAUSAL | ATTN_FLAG_SPLIT_TAIL)) return ATTN_ERR_UNSUPPORTED;
   if (Hkv < 1) return ATTN_ERR_INVALID_ARG;
   return attn_fwd_impl(q, k, v, out, layout, B, Hq, Sq, Sk, d, scale, rounding_mode, stream,
-                       kTimeoutNs, 0, 1, nullptr, 0, Hkv, (flags & ATTN_FLAG_CAUSAL) ? 1 : 0);
+                       kTimeoutNs, 0, 1, nullptr, 0, Hkv, (flags & ATTN_FLAG_CAUSAL) ? 1 : 0, 0,
+                       (flags & ATTN_FLAG_SPLIT_TAIL) ? 1 : 0);
 }
 
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
@@ -412,6 +495,8 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* out,
   p.head_group = p.causal ? head_group_of(B * Hq, total_k / B) : 1;
   p.dbg_poison = 0;
   p.n_items = static_cast<int>(B * Hq * n_qpairs);
+  p.item_base = 0;
+  p.early_dependents = 0;
 
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(B * Hq * n_qpairs);
@@ -458,6 +543,21 @@ int attn_fwd_splitkv_num_splits(int64_t B, int64_t H, int64_t Sq, int64_t Sk) {
   return static_cast<int>(s);
 }
 
+int attn_fwd_split_tail_items(int64_t B, int64_t Hq, int64_t Sq, int64_t Sk) {
+  if (B < 1 || Hq < 1 || Sq < 1 || Sk < 1) return ATTN_ERR_INVALID_ARG;
+  const int64_t kLim31 = (int64_t(1) << 31) - 1;
+  if (B > kLim31 || Hq > kLim31 || Sq > kLim31 || Sk > kLim31) return ATTN_ERR_TOO_LARGE;
+  if (B * Hq > kLim31 / qpairs_of(Sq)) return ATTN_ERR_TOO_LARGE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_NO_DEVICE;
+  }
+  const int st = device_ready(dev);
+  if (st != ATTN_OK) return st;
+  return static_cast<int>(pair_tail_items(dev, B * Hq * qpairs_of(Sq), kv_tiles_of(Sk)));
+}
+
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, int layout,
                      int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
                      int rounding_mode, int num_splits, void* workspace, int64_t workspace_bytes,
@@ -468,10 +568,11 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* out, int
 
 int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void* out, int layout,
                               int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
-                              int rounding_mode, void* stream, uint64_t timeout_ns) {
+                              int rounding_mode, void* stream, uint64_t timeout_ns, int flags) {
   if (timeout_ns == 0 || timeout_ns > kTimeoutNs) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_SPLIT_TAIL) return ATTN_ERR_UNSUPPORTED;
   return attn_fwd_impl(q, k, v, out, layout, B, H, Sq, Sk, d, scale, rounding_mode, stream,
-                       timeout_ns, 1, 1, nullptr, 0);
+                       timeout_ns, 1, 1, nullptr, 0, 0, 0, 0, (flags & ATTN_FLAG_SPLIT_TAIL) ? 1 : 0);
 }
 
 int attn_fwd_debug_build(void) { return ATTN_DEBUG ? 1 : 0; }

@@ -94,7 +94,9 @@ enum : int {
   kBarOFree = kBarQFree + 1,  // persistent, per query tile: the epilogue has read O
   kBarVChk = kBarOFree + kQTiles,  // key-limit variants: V of masked tile m checked (m < 3)
   kBarVLanded = kBarVChk + 3,      // key-limit variants: V of masked tile m is in the ring
-  kBarCount = kBarVLanded + 3
+  kBarPeerReady = kBarVLanded + 3,  // pair variant, rank 1: rank 0's ring is free for the exchange
+  kBarReceived = kBarPeerReady + 1, // pair variant, rank 0: rank 1's partial rows have arrived
+  kBarCount = kBarReceived + 1
 };
 
 constexpr int kOffQ = 0;
@@ -116,6 +118,12 @@ constexpr int kVRecKeyMask = 4, kVRecNan = 8, kVRecPos = kVRecNan + kBN * 4,
 constexpr int kOffVRec = (kSmemUsed + 15) & ~15;
 constexpr int kSmemBytesRowLimit = kOffVRec + kMaxMaskedTiles * kVRecWords * 4 + 1024;
 static_assert(kSmemBytesRowLimit <= 232448, "shared memory budget (key-limit variants)");
+// Pair variant: rank 1 sends its 256 unnormalised rows into rank 0's K/V ring
+// (256 x 512 bytes, the whole ring) and its (reference max, row sum) pairs here.
+constexpr int kOffPairMl = (kSmemUsed + 15) & ~15;
+constexpr int kSmemBytesPair = kOffPairMl + 2 * kBM * 8 + 1024;
+static_assert(kSmemBytesPair <= 232448, "shared memory budget (pair variant)");
+static_assert(kStages * kTileBytes == 2 * kBM * kD * 4, "the ring holds one CTA's fp32 rows");
 // The persistent variant also stages its output: 4 KiB per softmax warp (32
 // rows x 64 columns, one TMA box), so that the Q buffer can be refilled for the
 // next item while the current one is being stored.
@@ -152,6 +160,8 @@ struct Params {
   int head_group;   // causal: (batch, head) items scheduled together, longest first
   int dbg_poison;   // debug build only: report one failed check (tests the reporting)
   int n_items;      // persistent variant: work items; CTA c takes c, c + gridDim.x, ...
+  int item_base;    // pair variant: the work item of block 0 (CTA b takes item_base + b)
+  int early_dependents;  // base variant: a pair launch follows and may start early
 };
 
 // Bit 0: some wait timed out. Bit 1: a variable-length batch's offsets were
@@ -207,6 +217,23 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (honor_abort && *abort_flag) return false;
+    if (ptx::globaltimer() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(&g_attn_status, 1u);
+      return false;
+    }
+  }
+}
+
+// The same for a barrier that a CTA of the cluster arrives on remotely (acquire
+// at cluster scope); phase 0 only (each such barrier completes once).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, volatile int* abort_flag,
+                                                  unsigned long long timeout_ns) {
+  if (ptx::mbar_try_wait_cluster(bar, 0)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait_cluster(bar, 0)) return true;
+    if (*abort_flag) return false;
     if (ptx::globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
       atomicOr(&g_attn_status, 1u);
@@ -589,10 +616,12 @@ __device__ __forceinline__ Work work_of(const Params& p, int work_item) {
   return w;
 }
 
-// The CTA's own work item (one item per CTA).
-template <bool kCausal, bool kVarlen>
+// The CTA's own work item (one item per CTA; the pair variant's grid starts at
+// item_base).
+template <bool kCausal, bool kVarlen, bool kPair = false>
 __device__ __forceinline__ Work work_of(const Params& p) {
-  return work_of<kCausal, kVarlen>(p, blockIdx.x);
+  return work_of<kCausal, kVarlen>(
+      p, kPair ? p.item_base + static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
 }
 
 // First key tile of a work item in which some row of the CTA does not see every
@@ -616,9 +645,14 @@ __device__ __forceinline__ int first_masked_tile(const Work& w) {
 // item's Q loaded as soon as the current item's last S MMAs are done, and the
 // output stored through a staging area of its own; used for short key ranges,
 // where an item's fixed latency (first loads, epilogue, store) would otherwise
-// leave the SM idle. Each is compiled separately so that the other variants
-// carry none of it.
-template <bool kPartial, bool kCausal, bool kVarlen, bool kPersist = false>
+// leave the SM idle. kPair (whole key range, no mask only): the grid's CTAs
+// form 2-CTA clusters, each cluster one work item whose keys are split in two
+// halves (n_splits = 2); rank 1 sends its unnormalised rows to rank 0 through
+// distributed shared memory, and rank 0 merges them with its own and stores
+// the output; used for the last, partial wave of a launch, which then takes half
+// the time. Each is compiled separately so that the other variants carry none
+// of it.
+template <bool kPartial, bool kCausal, bool kVarlen, bool kPersist = false, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -634,6 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
 
   static_assert(!kPersist || (!kPartial && !kCausal && !kVarlen), "persistent: base path only");
+  static_assert(!kPair || (!kPartial && !kCausal && !kVarlen && !kPersist), "pair: base path only");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // A key limit per row (rising along the causal diagonal, or the sequence's
@@ -644,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Grid slots past the sequence's queries, and sequences with invalid
     // offsets, leave before anything is set up (the decision is the same for
     // every thread of the CTA).
-    const Work wk = work_of<kCausal, kVarlen>(p);
+    const Work wk = work_of<kCausal, kVarlen, kPair>(p);
     if (wk.bad) {
       if (threadIdx.x == 0) atomicOr(&g_attn_status, 2u);
       return;
@@ -654,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #if ATTN_DEBUG
   if (threadIdx.x == 0) {
     if (p.dbg_poison) dbg_ok(false);
-    const Work wk = work_of<kCausal, kVarlen>(p);
+    const Work wk = work_of<kCausal, kVarlen, kPair>(p);
     dbg_ok(wk.pair >= 0 && wk.pair < p.n_qpairs && wk.bh >= 0 && wk.bh < p.BH && wk.n_kv >= 1 &&
            wk.kv_head >= 0 && wk.kv_head * p.group < p.H);
     dbg_ok(kVarlen || wk.tile0 + wk.n_kv <= p.kv_tiles);
@@ -679,6 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(kBarVChk + m), 1);
       ptx::mbar_init(bar(kBarVLanded + m), 1);
     }
+    ptx::mbar_init(bar(kBarPeerReady), 1);
+    ptx::mbar_init(bar(kBarReceived), 2 * kBM);
     if (kRowLimit)
       for (int m = 0; m < kMaxMaskedTiles; ++m)
         reinterpret_cast<uint32_t*>(smem + kOffVRec)[m * kVRecWords] = 0;  // no non-finite V yet
@@ -687,8 +724,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_proxy_async_smem();
   }
   // The split variant's merge kernel may be scheduled as soon as every CTA of
-  // this grid has started (it waits for the whole grid before reading).
-  if constexpr (kPartial) ptx::launch_dependents();
+  // this grid has started (it waits for the whole grid before reading); so may
+  // the pair variant's launch after the base variant's full waves (it reads
+  // nothing they write, and waits for them only before it completes).
+  if constexpr (kPartial) {
+    ptx::launch_dependents();
+  } else if constexpr (!kCausal && !kVarlen && !kPersist && !kPair) {
+    if (p.early_dependents) ptx::launch_dependents();
+  }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tm_q);
     ptx::prefetch_tmap(&tm_k);
@@ -703,6 +746,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Pair variant: both CTAs' barriers are initialised before either arrives on
+  // the other's. Every thread of both CTAs reaches this point unconditionally.
+  if constexpr (kPair) ptx::cluster_sync();
 
   // Each role changes its register budget inside its own branch, so that the
   // budget of every instruction is known where it is compiled.
@@ -765,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         if (lane == 0) {
-          const Work wk = work_of<kCausal, kVarlen>(p);
+          const Work wk = work_of<kCausal, kVarlen, kPair>(p);
           const int pair = wk.pair, head = wk.head, batch = wk.batch, tile0 = wk.tile0, n_kv = wk.n_kv;
           const int kv_head = wk.kv_head, q_base = wk.q_base, k_base = wk.k_base;
           int issued = 0;  // ring fills started so far (fill i goes to stage i % kStages)
@@ -879,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ktile += n_kv;
           }
         } else {
-          const Work wk = work_of<kCausal, kVarlen>(p);
+          const Work wk = work_of<kCausal, kVarlen, kPair>(p);
           const int n_kv = wk.n_kv;
           // Masked key tiles (key-limit variants): V is checked first.
           const int jm = kRowLimit ? first_masked_tile<kCausal>(wk) : n_kv;
@@ -949,7 +995,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Wait until every MMA issued so far has finished (immediate on the normal
         // path, where the softmax warps have already waited for the last ones).
         ptx::mma_commit(bar(kBarDrain));
-        wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
+        const bool drained = wait_bounded(bar(kBarDrain), 0, abort_flag, p.timeout_ns, false);
+        // Pair variant, rank 0: no MMA or copy uses the ring any more; rank 1 may
+        // write its rows into it.
+        if (kPair && drained && ptx::cluster_ctarank() == 0)
+          ptx::mbar_arrive_cluster(ptx::map_to_rank(bar(kBarPeerReady), 1));
       }
       __syncwarp();
     } else if constexpr (kRowLimit) {
@@ -963,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // at barriers of both warps (with a reduction), so neither can leave while
       // the other waits.
       const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..63
-      const Work wk = work_of<kCausal, kVarlen>(p);
+      const Work wk = work_of<kCausal, kVarlen, kPair>(p);
       const int jm = first_masked_tile<kCausal>(wk);
       dbg_ok(wk.n_kv - jm <= kMaxMaskedTiles);
       for (int m = 0; jm + m < wk.n_kv && m < kMaxMaskedTiles; ++m) {
@@ -1208,7 +1258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int n_kv, row_lim;
       {
-        const Work wk = work_of<kCausal, kVarlen>(p);
+        const Work wk = work_of<kCausal, kVarlen, kPair>(p);
         n_kv = wk.n_kv;  // key tiles of this CTA
         // Number of keys this row sees, counted from the sequence's key 0: the
         // causal limit (capped at Sk, which also hides the ragged tail from the
@@ -1225,7 +1275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of kernel parameters and the block index, which keeps the compiler's
         // register allocation of this loop free of spills.
         const bool last = (j == n_kv - 1) && (p.kv_tail < kBN) &&
-                          (!kPartial || static_cast<int>(blockIdx.x % p.n_splits) == p.n_splits - 1);
+                          (kPair ? (blockIdx.x & 1u) != 0
+                                 : (!kPartial ||
+                                    static_cast<int>(blockIdx.x % p.n_splits) == p.n_splits - 1));
         // Masked tile: the ragged last tile; with the causal mask every tile, each
         // row hiding the keys beyond its own limit (a tile it fully sees loses
         // nothing). One path for all tiles keeps the loop's registers spill-free.
@@ -1310,7 +1362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // then keeps none of its fields live across the loop above.
       int bx = static_cast<int>(blockIdx.x);
       asm volatile("" : "+r"(bx));
-      const Work wk = work_of<kCausal, kVarlen>(p, bx);
+      const Work wk = work_of<kCausal, kVarlen>(p, kPair ? p.item_base + bx : bx);
       if (kPartial && ok) {
         // Split epilogue: this row's unnormalised fp32 output, the running max it is
         // relative to, and its row sum.
@@ -1333,6 +1385,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (ok) {
         ptx::tc_fence_after();
         fold_last(tO, acc);
+        if constexpr (kPair) {
+          // The two halves of the key range: rank 1 sends, rank 0 merges. Row R of
+          // the CTA (0..255) is 512 bytes of the ring at R * 512, its 16-byte chunk
+          // i at position i ^ (R & 31) (so a warp's 32 rows hit distinct banks).
+          const int R = t * kBM + row;
+          const uint32_t row_s = sRing + static_cast<uint32_t>(R) * 512u;
+          const uint32_t ml_s = sbase + kOffPairMl + static_cast<uint32_t>(R) * 8u;
+          if (ptx::cluster_ctarank() == 1) {
+            // Wait (bounded) until rank 0's ring is free, then write this row there.
+            const bool ready = wait_bounded_cluster(bar(kBarPeerReady), abort_flag, p.timeout_ns);
+            if (ready) {
+              const uint32_t dst = ptx::map_to_rank(row_s, 0);
+#pragma unroll
+              for (int i = 0; i < kD / 4; ++i) {
+                const uint64_t a = acc[2 * i], b = acc[2 * i + 1];
+                ptx::st_cluster_v4(dst + ((static_cast<uint32_t>(i) ^ (R & 31)) << 4),
+                                   static_cast<uint32_t>(a), static_cast<uint32_t>(a >> 32),
+                                   static_cast<uint32_t>(b), static_cast<uint32_t>(b >> 32));
+              }
+              ptx::st_cluster_v2(ptx::map_to_rank(ml_s, 0), __float_as_uint(m_used),
+                                 __float_as_uint(l));
+              ptx::mbar_arrive_cluster(ptx::map_to_rank(bar(kBarReceived), 0));
+            }
+            ok = false;  // rank 1 stores nothing
+          } else {
+            // Wait (bounded) for rank 1's 256 rows, then merge row R: both halves'
+            // sums are relative to their own reference m (0 while m = -Inf); with
+            // M = the larger one, O = 2^(m0 - M) O0 + 2^(m1 - M) O1 and likewise l.
+            const bool got = wait_bounded_cluster(bar(kBarReceived), abort_flag, p.timeout_ns);
+            ok = got;
+            if (got) {
+              const uint2 ml = *reinterpret_cast<const uint2*>(smem + (ml_s - sbase));
+              const float m1 = __uint_as_float(ml.x), l1 = __uint_as_float(ml.y);
+              const float neg_inf_m = -__int_as_float(0x7F800000);
+              float M = fmaxf(m_used, m1);
+              if (M == neg_inf_m) M = 0.f;
+              const float w0 = ptx::ex2(m_used - M), w1 = ptx::ex2(m1 - M);
+              // The same operations in the same order as the split-key combine
+              // (an fma onto +0 first, then one onto that), so that both give the
+              // same bits.
+              l = fmaf(l1, w1, fmaf(l, w0, 0.f));
+              const uint64_t w0_2 = ptx::f2_pack(w0, w0), w1_2 = ptx::f2_pack(w1, w1);
+              const uint64_t zero2 = 0;
+#pragma unroll
+              for (int i = 0; i < kD / 4; ++i) {
+                const uint4 x =
+                    ptx::ld_shared_v4(row_s + ((static_cast<uint32_t>(i) ^ (R & 31)) << 4));
+                acc[2 * i] = ptx::f2_fma((static_cast<uint64_t>(x.y) << 32) | x.x, w1_2,
+                                         ptx::f2_fma(acc[2 * i], w0_2, zero2));
+                acc[2 * i + 1] = ptx::f2_fma((static_cast<uint64_t>(x.w) << 32) | x.z, w1_2,
+                                             ptx::f2_fma(acc[2 * i + 1], w0_2, zero2));
+              }
+            }
+          }
+        }
+      }
+      if (!kPartial && ok) {
         // Normalise, round, stage in the (now free) Q tile buffer with the TMA
         // 128-byte swizzle, and store this warp's 32 rows with two TMA boxes.
         const uint32_t stage_base = sQ + t * kTileBytes;
@@ -1443,6 +1552,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  // Pair variant: the grid completes only after the launch it may overlap (the
+  // full waves of the same call), so that later work on the stream sees both;
+  // and neither CTA leaves while the other may still use its shared memory.
+  // Every thread reaches this point (all waits above are bounded).
+  if constexpr (kPair) {
+    ptx::grid_dependency_wait();
+    ptx::cluster_sync();
   }
 }
 

@@ -77,8 +77,9 @@ enum {
  *
  * Asynchronous: returns after the launch; `out` is valid once the stream has
  * reached the call. All pointers must be 16-byte aligned. The call allocates
- * no device memory. Results are bit-identical from run to run. Thread-safe.
- * Returns ATTN_OK or a negative status code.
+ * no device memory. Results are bit-identical from run to run, and each
+ * (batch, head, query row)'s result is independent of the rest of the call.
+ * Thread-safe. Returns ATTN_OK or a negative status code.
  *
  * Schedule (invisible in the result): one CTA per (batch, head, pair of
  * 128-row query tiles); when Sk <= 2048 and there are more such items than
@@ -90,7 +91,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* out, int layout,
              int rounding_mode, void* stream);
 
 /* Flags of attn_fwd_ex. */
-enum { ATTN_FLAG_CAUSAL = 1 };
+enum { ATTN_FLAG_CAUSAL = 1, ATTN_FLAG_SPLIT_TAIL = 2 };
 
 /*
  * attn_fwd_ex - attn_fwd with two of the follow-on steps the pages list as
@@ -108,11 +109,37 @@ enum { ATTN_FLAG_CAUSAL = 1 };
  *            all: a NaN or infinity in V at a key a query does not see does not
  *            reach that query's output, while a query that sees it gets NaN or
  *            that infinity in the column.
+ *            ATTN_FLAG_SPLIT_TAIL (without the mask; no effect with it): when
+ *            the items of the launch's last, partial wave fit on the GPU at once
+ *            as pairs of CTAs (2-CTA clusters) and the key range has at least 8
+ *            tiles of 128 keys (more than 16 when there are more items than
+ *            SMs), each of those items runs on a pair, each CTA taking half of
+ *            its key tiles, merged on chip with the same arithmetic as
+ *            attn_fwd_splitkv with 2 splits. The last wave then takes about
+ *            half as long. The price: an item's bits then depend on how many
+ *            items the call has (they stay within the numerics contract and the
+ *            same from run to run). Without the flag every item's result is
+ *            independent of the rest of the call: a sub-batch or a slice of the
+ *            heads gives the same bits as the whole call.
  * Other arguments, ownership, errors and the numerics contract as attn_fwd.
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layout, int64_t B,
                 int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Sk, int64_t d, float scale,
                 int rounding_mode, int flags, void* stream);
+
+/*
+ * attn_fwd_split_tail_items - how many of the (batch, head, query-tile pair)
+ * items of an attn_fwd_ex call of this size with ATTN_FLAG_SPLIT_TAIL (and no
+ * mask) run on pairs of CTAs on the current device: 0 when the flag changes
+ * nothing. When the result is above 0 and below the item count
+ * B * Hq * ceil(Sq / 256), the call makes two kernel launches (the full waves,
+ * then the pairs); otherwise one.
+ *
+ * Returns the count (>= 0), ATTN_ERR_INVALID_ARG if a size is below 1,
+ * ATTN_ERR_TOO_LARGE beyond the launch limits of attn_fwd, or
+ * ATTN_ERR_NO_DEVICE / ATTN_ERR_ARCH for the current device. Launches nothing.
+ */
+int attn_fwd_split_tail_items(int64_t B, int64_t Hq, int64_t Sq, int64_t Sk);
 
 /*
  * Split-KV: the same operation with each query tile's key range cut into
@@ -310,7 +337,9 @@ int attn_fwd_last_error(void);
  * attn_fwd_timeout_selftest - exercises the failure path on a real GPU.
  *
  * Same arguments, checks and launch as attn_fwd, plus a wait limit in
- * nanoseconds (1 .. 2e9), but the kernel withholds one of its own internal
+ * nanoseconds (1 .. 2e9) and flags (0 or ATTN_FLAG_SPLIT_TAIL, which runs the
+ * launch as attn_fwd_ex with that flag would; any other bit gives
+ * ATTN_ERR_UNSUPPORTED), but the kernel withholds one of its own internal
  * signals (the tensor-core warp never announces query tile 0's first S tile),
  * so a device-side wait must run out. Every role of the kernel then stops,
  * waits for the copies and matrix products it started, frees its tensor memory
@@ -320,7 +349,7 @@ int attn_fwd_last_error(void);
  */
 int attn_fwd_timeout_selftest(const void* q, const void* k, const void* v, void* out, int layout,
                               int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t d, float scale,
-                              int rounding_mode, void* stream, uint64_t timeout_ns);
+                              int rounding_mode, void* stream, uint64_t timeout_ns, int flags);
 
 /* Library version, as MAJOR*10000 + MINOR*100 + PATCH. */
 int attn_fwd_version(void);

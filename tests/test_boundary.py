@@ -87,11 +87,23 @@ def test_timeout_selftest_validation(lib):
     assert attn.attn_fwd_timeout_selftest_raw(*args, 0, 3_000_000_000) == attn.ATTN_ERR_INVALID_ARG
     bad = (0,) + args[1:]
     assert attn.attn_fwd_timeout_selftest_raw(*bad, 0, 10_000_000) == attn.ATTN_ERR_INVALID_ARG
+    # Flags: the tail split only (the causal mask is not a mode of this test entry).
+    assert (attn.attn_fwd_timeout_selftest_raw(*args, 0, 10_000_000, attn.ATTN_FLAG_CAUSAL)
+            == attn.ATTN_ERR_UNSUPPORTED)
+    assert (attn.attn_fwd_timeout_selftest_raw(*args, 0, 10_000_000, attn.ATTN_FLAG_SPLIT_TAIL)
+            == attn.ATTN_ERR_NO_DEVICE)
 
 
 def _split(q=A, k=2 * A, v=3 * A, o=4 * A, B=1, H=2, Sq=256, Sk=1000, splits=2, ws=8 * A,
            ws_bytes=1 << 24):
     return attn.attn_fwd_splitkv_raw(q, k, v, o, 0, B, H, Sq, Sk, 128, 0.088, 0, splits, ws, ws_bytes, 0)
+
+
+def test_split_tail_items_validation(lib):
+    assert attn.split_tail_items(0, 1, 256, 256) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.split_tail_items(1 << 31, 1, 256, 256) == attn.ATTN_ERR_TOO_LARGE
+    assert attn.split_tail_items(1 << 20, 1 << 20, 256, 256) == attn.ATTN_ERR_TOO_LARGE
+    assert attn.split_tail_items(1, 8, 4096, 32768) == attn.ATTN_ERR_NO_DEVICE  # valid; no GPU
 
 
 def test_splitkv_workspace_bytes(lib):
@@ -143,7 +155,9 @@ def test_splitkv_valid_call_without_gpu_reports_no_device(lib):
 @pytest.mark.parametrize("Hq,Hkv,flags,status", [
     (8, 3, 0, attn.ATTN_ERR_INVALID_ARG),     # Hq not a multiple of Hkv
     (8, 0, 0, attn.ATTN_ERR_INVALID_ARG),
-    (8, 2, 2, attn.ATTN_ERR_UNSUPPORTED),     # unknown flag
+    (8, 2, 4, attn.ATTN_ERR_UNSUPPORTED),     # unknown flag
+    (8, 2, attn.ATTN_FLAG_SPLIT_TAIL, attn.ATTN_ERR_NO_DEVICE),  # accepted; no GPU here
+    (8, 2, attn.ATTN_FLAG_SPLIT_TAIL | attn.ATTN_FLAG_CAUSAL, attn.ATTN_ERR_NO_DEVICE),
 ])
 def test_ex_validation(lib, Hq, Hkv, flags, status):
     assert attn.attn_fwd_ex_raw(A, 2 * A, 3 * A, 4 * A, 0, 1, Hq, Hkv, 256, 256, 128, 0.088, 0,

@@ -32,6 +32,8 @@ int main(void) {
                      ATTN_LAYOUT_BHSD, 1, 6, 4, 16, 16, 128, 0.1f, ATTN_ROUND_RTNA,
                      ATTN_FLAG_CAUSAL, NULL) == ATTN_ERR_INVALID_ARG);
   EXPECT(attn_fwd_splitkv_workspace_bytes(1, 2, 256, 1000, 128, 2) > 0);
+  EXPECT(attn_fwd_split_tail_items(0, 1, 1, 1) == ATTN_ERR_INVALID_ARG);
+  EXPECT(ATTN_FLAG_SPLIT_TAIL == 2 && (ATTN_FLAG_SPLIT_TAIL & ATTN_FLAG_CAUSAL) == 0);
   EXPECT(attn_fwd_host_workspace_bytes(1, 2, 2, 256, 256, 128) == 4 * 2 * 256 * 256);
   EXPECT(attn_fwd_debug_build() == 0 || attn_fwd_debug_build() == 1);
   printf("%s\n", fails ? "C-ABI FAILED" : "C-ABI OK");

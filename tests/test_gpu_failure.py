@@ -24,8 +24,10 @@ def _library():
     attn.load_library()
 
 
-@pytest.mark.parametrize("Sk", [200, 1000])
-def test_withheld_signal_times_out_cleanly(Sk):
+# Sk = 1000 (8 key tiles, 2 items) with the tail split runs the pair variant:
+# both CTAs of each cluster give up, skip the exchange and meet at the end.
+@pytest.mark.parametrize("Sk,flags", [(200, 0), (1000, 0), (1000, attn.ATTN_FLAG_SPLIT_TAIL)])
+def test_withheld_signal_times_out_cleanly(Sk, flags):
     w = inputs.Workload("fail", "bhsd", 1, 2, 256, Sk, seed=90)
     q, k, v = inputs.make_qkv(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
@@ -35,7 +37,7 @@ def test_withheld_signal_times_out_cleanly(Sk):
     t0 = time.time()
     st = attn.attn_fwd_timeout_selftest_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
                                             out.data_ptr(), 0, 1, 2, 256, Sk, 128,
-                                            inputs.default_scale(), 0, stream, 20_000_000)
+                                            inputs.default_scale(), 0, stream, 20_000_000, flags)
     assert st == attn.ATTN_OK
     torch.cuda.synchronize()
     assert time.time() - t0 < 10.0
