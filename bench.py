@@ -596,7 +596,8 @@ def run_ours(args, w):
                       "timed_region_mean": avg_launch_ms, "timed_region_n": len(launch_ms)},
         "roofline": {"bound": bound, "achieved": achieved, "peak": roof_peak, "unit": roof_unit,
                      "frac": achieved / roof_peak,
-                     "traffic": args.traffic if args.traffic is not None else _recorded_traffic(w.name),
+                     "traffic": (args.traffic if args.traffic is not None else
+                                 _recorded_traffic(w.name + ("+split_tail" if split_tail else ""))),
                      "peak_kind": (f"{'sustained' if sustained else 'burst'} dense bf16 ({peak_src})"
                                    if bound == "tensor" else f"HBM copy bandwidth ({peak_src})"),
                      "algorithmic_bytes": w.io_bytes,
