@@ -1,24 +1,29 @@
 // attn_host.cu - attention on host buffers, declared in include/attn_fwd.h.
 //
 // The caller's inputs and output live in host memory (page-locked for the
-// copies to overlap anything). The problem is cut into chunks that are
-// contiguous in every tensor; each chunk's inputs go to the device on one
-// internal stream, its kernel runs on one of two compute streams once they have
-// landed, and its output comes back on a third stream once the kernel is done.
-// So chunk i's kernel overlaps chunk i+1's upload and chunk i-1's download, and
-// neighbouring kernels can fill each other's tail waves. Events order
-// everything; nothing on the host waits. The device tensors are the caller's
-// workspace, laid out exactly like the host tensors.
+// copies to overlap anything). The problem is cut into chunks; each chunk's
+// inputs go to the device on one internal stream, its kernel runs on one of two
+// compute streams once they have landed, and its output comes back on a third
+// stream once the kernel is done. So chunk i's kernel overlaps chunk i+1's
+// upload and chunk i-1's download, and neighbouring kernels can fill each
+// other's tail waves. Events order everything; nothing on the host waits. The
+// device tensors are in the caller's workspace, each chunk's share packed
+// densely there in the caller's layout.
 //
 // Chunks (every chunk attends only within itself, so each is an attn_fwd_ex
-// call on sub-tensors):
+// call on its own dense sub-tensors):
 //   BHSD: (b, h) pairs are contiguous blocks, and (B, H, S, d) is the same memory
 //         as (1, B*H, S, d); chunks are runs of whole key/value heads with their
 //         query heads (a multiple of the group size).
 //   BSHD: batch entries are contiguous blocks; chunks are runs of batch
-//         entries, or, with few entries, runs of query rows of one entry (the
-//         rows of an entry are contiguous, its K/V go up with its first chunk).
-//         A row chunk [s0, s1) of a causal problem is the causal problem with
+//         entries. With fewer entries than chunks, each entry is cut into runs
+//         of key/value heads with their query heads: strided in the caller's
+//         tensors (one row of the run's heads per token), copied with 2-D copies
+//         and packed densely on the device, so that the first chunk's upload is
+//         one run's Q, K and V, and each chunk's CTAs share one run's K/V in L2.
+//         With a single key/value head, the entry is cut into runs of query rows
+//         instead (contiguous; the entry's K/V go up with its first chunk). A
+//         row chunk [s0, s1) of a causal problem is the causal problem with
 //         Sq' = s1 - s0 and Sk' = s1 + Sk - Sq: row i' sees keys up to
 //         i' + s0 + Sk - Sq, the same keys as row s0 + i' of the whole problem.
 //   packed variable-length batch (attn_fwd_varlen_host): runs of whole
@@ -79,12 +84,36 @@ int setup(DeviceStreams& d) {
   return ATTN_OK;
 }
 
-// One chunk: byte ranges of the four tensors (same offsets on host and device)
+// One tensor's share of a chunk: `rows` runs of `width` bytes, `pitch` bytes
+// apart, from byte `host` of the caller's tensor, packed densely from byte `dev`
+// of the device tensor. rows == 0: already on the device (K/V of a row chunk).
+struct Span {
+  int64_t host, dev, width, rows, pitch;
+};
+
+// A contiguous share: the same offset on host and device.
+Span flat(int64_t off, int64_t bytes, bool copy = true) {
+  return {off, off, bytes, copy ? 1 : 0, bytes};
+}
+
+// One chunk: its shares of Q (and of O, which has Q's shape), of K and V (alike),
 // and the sub-problem they form.
 struct Chunk {
-  int64_t q_off, q_bytes, kv_off, kv_bytes;  // kv_bytes 0: K/V already uploaded
+  Span q, kv;
   int64_t B, Hq, Hkv, Sq, Sk;
 };
+
+bool copy_span(char* dst_base, const char* src_base, const Span& s, cudaMemcpyKind kind,
+               cudaStream_t st) {
+  if (s.rows == 0) return true;
+  const bool up = kind == cudaMemcpyHostToDevice;
+  char* dst = dst_base + (up ? s.dev : s.host);
+  const char* src = src_base + (up ? s.host : s.dev);
+  if (s.rows == 1 || s.pitch == s.width)
+    return cudaMemcpyAsync(dst, src, s.width * s.rows, kind, st) == cudaSuccess;
+  return cudaMemcpy2DAsync(dst, up ? s.width : s.pitch, src, up ? s.pitch : s.width, s.width,
+                           s.rows, kind, st) == cudaSuccess;
+}
 
 // Splits the problem into at most kMaxChunks chunks of at least kCtasPerChunk
 // CTAs (one CTA per 256 query rows of one head) where possible.
@@ -101,8 +130,9 @@ std::vector<Chunk> plan(int layout, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
     const int64_t n = want < units ? want : units;
     for (int64_t c = 0; c < n; ++c) {
       const int64_t u0 = units * c / n, u1 = units * (c + 1) / n;
-      out.push_back({u0 * group * Sq * row, (u1 - u0) * group * Sq * row, u0 * Sk * row,
-                     (u1 - u0) * Sk * row, 1, (u1 - u0) * group, u1 - u0, Sq, Sk});
+      out.push_back({flat(u0 * group * Sq * row, (u1 - u0) * group * Sq * row),
+                     flat(u0 * Sk * row, (u1 - u0) * Sk * row), 1, (u1 - u0) * group, u1 - u0,
+                     Sq, Sk});
     }
     return out;
   }
@@ -110,15 +140,37 @@ std::vector<Chunk> plan(int layout, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
   if (want <= B) {
     for (int64_t c = 0; c < want; ++c) {
       const int64_t b0 = B * c / want, b1 = B * (c + 1) / want;
-      out.push_back({b0 * q_batch, (b1 - b0) * q_batch, b0 * kv_batch, (b1 - b0) * kv_batch,
+      out.push_back({flat(b0 * q_batch, (b1 - b0) * q_batch), flat(b0 * kv_batch, (b1 - b0) * kv_batch),
                      b1 - b0, Hq, Hkv, Sq, Sk});
     }
     return out;
   }
-  // Fewer batch entries than chunks: cut each entry's query rows. Boundaries are
+  // Runs per entry: enough for `want` chunks, but at most kMaxChunks in all.
+  int64_t per = (want + B - 1) / B;
+  if (per > kMaxChunks / B) per = kMaxChunks / B;
+  if (per < 1) per = 1;
+  if (Hkv > 1) {
+    // Runs of key/value heads of each entry, with their query heads; each run's
+    // rows are packed densely on the device, one run after the other.
+    const int64_t group = Hq / Hkv;
+    const int64_t n = per < Hkv ? per : Hkv;
+    int64_t dq = 0, dkv = 0;
+    for (int64_t b = 0; b < B; ++b) {
+      for (int64_t c = 0; c < n; ++c) {
+        const int64_t u0 = Hkv * c / n, u1 = Hkv * (c + 1) / n;
+        const int64_t qw = (u1 - u0) * group * row, kvw = (u1 - u0) * row;
+        out.push_back({{b * q_batch + u0 * group * row, dq, qw, Sq, Hq * row},
+                       {b * kv_batch + u0 * row, dkv, kvw, Sk, Hkv * row}, 1, (u1 - u0) * group,
+                       u1 - u0, Sq, Sk});
+        dq += qw * Sq;
+        dkv += kvw * Sk;
+      }
+    }
+    return out;
+  }
+  // A single key/value head: cut each entry's query rows. Boundaries are
   // multiples of 256 rows; under the causal mask the first chunk of an entry
   // also takes every row that sees no key (Sk' = s1 + Sk - Sq must be >= 1).
-  const int64_t per = (want + B - 1) / B;
   for (int64_t b = 0; b < B; ++b) {
     int64_t s0 = 0;
     bool first = true;
@@ -127,8 +179,8 @@ std::vector<Chunk> plan(int layout, int64_t B, int64_t Hq, int64_t Hkv, int64_t 
       if (s1 > Sq) s1 = Sq;
       if (s1 <= s0) continue;
       if (causal && s1 + Sk - Sq < 1) continue;  // merge into the next chunk
-      out.push_back({b * q_batch + s0 * Hq * row, (s1 - s0) * Hq * row, b * kv_batch,
-                     first ? kv_batch : 0, 1, Hq, Hkv, s1 - s0,
+      out.push_back({flat(b * q_batch + s0 * Hq * row, (s1 - s0) * Hq * row),
+                     flat(b * kv_batch, kv_batch, first), 1, Hq, Hkv, s1 - s0,
                      causal ? s1 + Sk - Sq : Sk});
       first = false;
       s0 = s1;
@@ -154,8 +206,10 @@ std::vector<SeqChunk> plan_varlen(const int32_t* cq, int64_t B, int64_t Hq) {
     const int64_t sq = cq[b + 1] - cq[b];
     acc += Hq * qpairs(sq);
     max_sq = sq > max_sq ? sq : max_sq;
+    // The last chunk takes every remaining sequence (also ones without queries),
+    // so there are at most `want` chunks.
     const int64_t goal = total * (static_cast<int64_t>(out.size()) + 1) / want;
-    if (acc >= goal || b == B - 1) {
+    if ((acc >= goal && static_cast<int64_t>(out.size()) + 1 < want) || b == B - 1) {
       out.push_back({b0, b + 1, max_sq});
       b0 = b + 1;
       max_sq = 0;
@@ -207,6 +261,7 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* out, int la
 
   const bool causal = (flags & ATTN_FLAG_CAUSAL) != 0;
   const std::vector<Chunk> chunks = plan(layout, B, Hq, Hkv, Sq, Sk, causal);
+  if (chunks.empty() || chunks.size() > static_cast<size_t>(kMaxChunks)) return ATTN_ERR_LAUNCH;
   const int64_t q_region = round_up(B * Hq * Sq * 256, kAlign);
   const int64_t kv_region = round_up(B * Hkv * Sk * 256, kAlign);
   char* wq = static_cast<char*>(workspace);
@@ -227,26 +282,21 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* out, int la
   for (size_t i = 0; i < chunks.size() && status == ATTN_OK; ++i) {
     const Chunk& c = chunks[i];
     const cudaStream_t cs = ds.comp[i & 1];
-    ok = cudaMemcpyAsync(wq + c.q_off, hq + c.q_off, c.q_bytes, cudaMemcpyHostToDevice, ds.in) ==
-         cudaSuccess;
-    if (ok && c.kv_bytes > 0)
-      ok = cudaMemcpyAsync(wk + c.kv_off, hk + c.kv_off, c.kv_bytes, cudaMemcpyHostToDevice,
-                           ds.in) == cudaSuccess &&
-           cudaMemcpyAsync(wv + c.kv_off, hv + c.kv_off, c.kv_bytes, cudaMemcpyHostToDevice,
-                           ds.in) == cudaSuccess;
+    ok = copy_span(wq, hq, c.q, cudaMemcpyHostToDevice, ds.in) &&
+         copy_span(wk, hk, c.kv, cudaMemcpyHostToDevice, ds.in) &&
+         copy_span(wv, hv, c.kv, cudaMemcpyHostToDevice, ds.in);
     ok = ok && cudaEventRecord(ds.landed[i], ds.in) == cudaSuccess &&
          cudaStreamWaitEvent(cs, ds.landed[i], 0) == cudaSuccess;
     if (!ok) {
       status = ATTN_ERR_LAUNCH;
       break;
     }
-    status = attn_fwd_ex(wq + c.q_off, wk + c.kv_off, wv + c.kv_off, wo + c.q_off, layout, c.B,
+    status = attn_fwd_ex(wq + c.q.dev, wk + c.kv.dev, wv + c.kv.dev, wo + c.q.dev, layout, c.B,
                          c.Hq, c.Hkv, c.Sq, c.Sk, d, scale, rounding_mode, flags, cs);
     if (status != ATTN_OK) break;
     ok = cudaEventRecord(ds.computed[i], cs) == cudaSuccess &&
          cudaStreamWaitEvent(ds.out, ds.computed[i], 0) == cudaSuccess &&
-         cudaMemcpyAsync(ho + c.q_off, wo + c.q_off, c.q_bytes, cudaMemcpyDeviceToHost, ds.out) ==
-             cudaSuccess;
+         copy_span(ho, wo, c.q, cudaMemcpyDeviceToHost, ds.out);
     if (!ok) status = ATTN_ERR_LAUNCH;
   }
   // The caller's stream waits for everything enqueued above, also after an error.
@@ -307,6 +357,7 @@ int attn_fwd_varlen_host(const void* q, const void* k, const void* v, void* out,
   if (st0 != ATTN_OK) return st0;
 
   const std::vector<SeqChunk> chunks = plan_varlen(cu_seqlens_q, B, Hq);
+  if (chunks.empty() || chunks.size() > static_cast<size_t>(kMaxChunks)) return ATTN_ERR_LAUNCH;
   const int64_t q_region = round_up(total_q * Hq * 256, kAlign);
   const int64_t kv_region = round_up(total_k * Hkv * 256, kAlign);
   const int64_t cu_region = round_up((B + 1) * 4, kAlign);

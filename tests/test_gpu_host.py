@@ -29,13 +29,23 @@ def _qkv(layout, B, Hq, Hkv, Sq, Sk, seed):
 
 
 # Shapes large enough that the planner cuts several chunks (>= 512 CTAs of 256
-# query rows x one head): BSHD row chunks of one entry, BSHD batch runs, BHSD
-# head runs with grouped heads, and causal row chunks with Sq > Sk, where the
-# first chunk must take every row that sees no key.
+# query rows x one head):
+# - BSHD runs of key/value heads of one entry (strided on the host, packed on the
+#   device), with grouped heads and causal;
+# - BSHD row chunks of one entry (a single key/value head), also causal with
+#   Sq > Sk, where the first chunk must take every row that sees no key;
+# - BSHD batch runs;
+# - BHSD head runs with grouped heads.
+# The 3- and 7-entry shapes ask for 8 chunks with fewer entries: the planner
+# must stay within its 8 chunks.
 @pytest.mark.parametrize("layout,B,Hq,Hkv,Sq,Sk,causal", [
     ("bshd", 1, 16, 16, 8192, 3000, False),
     ("bshd", 1, 16, 4, 8192, 5000, True),
     ("bshd", 1, 16, 16, 8200, 700, True),      # Sq > Sk: the first 7500 rows see no key
+    ("bshd", 1, 16, 1, 8200, 700, True),       # one key/value head: row chunks
+    ("bshd", 3, 32, 32, 5632, 512, False),     # 2 head runs per entry, 6 chunks
+    ("bshd", 3, 32, 1, 5632, 512, True),       # 2 row chunks per entry
+    ("bshd", 7, 16, 16, 4864, 300, False),     # one chunk per entry
     ("bshd", 4, 8, 8, 2304, 2304, True),
     ("bhsd", 2, 16, 8, 4096, 1000, False),
     ("bhsd", 3, 12, 3, 2500, 2600, True),
@@ -88,6 +98,22 @@ def test_varlen_host_equals_device_call_bitwise(causal):
                                     torch.from_numpy(cq), torch.from_numpy(ck), causal=causal)
     want = attn.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cq).cuda(),
                                 torch.from_numpy(ck).cuda(), 4096, causal=causal)
+    torch.cuda.synchronize()
+    assert attn.attn_fwd_last_error() == attn.ATTN_OK
+    assert torch.equal(got.view(torch.int16), want.cpu().view(torch.int16))
+
+
+def test_varlen_host_trailing_sequences_without_queries():
+    # 2048 CTAs ask for 8 chunks, reached at the last sequence with queries; the
+    # sequences after it (no queries) join the last chunk.
+    lens = ((4096, 4096),) * 8 + ((0, 300), (0, 10))
+    w = inputs.Workload("vh", "thd", len(lens), 16, 4096, 4096, seed=1312, hkv=16, seqlens=lens)
+    q, k, v = inputs.make_qkv(w)
+    cq, ck = w.cu_seqlens
+    got = attn.attn_fwd_varlen_host(q.pin_memory(), k.pin_memory(), v.pin_memory(),
+                                    torch.from_numpy(cq), torch.from_numpy(ck))
+    want = attn.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(cq).cuda(),
+                                torch.from_numpy(ck).cuda(), 4096)
     torch.cuda.synchronize()
     assert attn.attn_fwd_last_error() == attn.ATTN_OK
     assert torch.equal(got.view(torch.int16), want.cpu().view(torch.int16))
