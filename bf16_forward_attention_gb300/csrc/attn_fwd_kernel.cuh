@@ -308,18 +308,26 @@ __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
 }
 
 // Two fp32 results of arithmetic -> packed bf16x2 (x0 in bits 0..15), rounded as
-// round_bf16_bits does, with the mode's constants hoisted out of the element
-// loop: bias 0x7FFF plus the kept lowest bit (lsb_mask 1) for RTNE, 0x8000 for
-// RTNA, 0 for RTZ, added before the upper halves are taken. A NaN produced by
-// fp32 arithmetic on this GPU is the positive pattern 0x7FFFFFFF: as a signed
-// integer it is above 0x7FC00000, so a signed min turns it (and only it: every
-// other value, negative ones included, is not above) into 0x7FC00000, which
-// every mode rounds to the one NaN pattern 0x7FC0.
-__device__ __forceinline__ uint32_t round_pair_bf16(float x0, float x1, uint32_t bias,
-                                                    uint32_t lsb_mask) {
+// round_bf16_bits does for RTNA (bias 0x8000) or RTZ (bias 0), the bias added
+// before the upper halves are taken. A NaN produced by fp32 arithmetic on this
+// GPU is the positive pattern 0x7FFFFFFF: as a signed integer it is above
+// 0x7FC00000, so a signed min turns it (and only it: every other value, negative
+// ones included, is not above) into 0x7FC00000, which both modes round to the one
+// NaN pattern 0x7FC0.
+__device__ __forceinline__ uint32_t round_pair_bf16(float x0, float x1, uint32_t bias) {
   const uint32_t u0 = static_cast<uint32_t>(min(__float_as_int(x0), 0x7FC00000));
   const uint32_t u1 = static_cast<uint32_t>(min(__float_as_int(x1), 0x7FC00000));
-  return ptx::prmt_hi16(u0 + bias + ((u0 >> 16) & lsb_mask), u1 + bias + ((u1 >> 16) & lsb_mask));
+  return ptx::prmt_hi16(u0 + bias, u1 + bias);
+}
+
+// The same for RTNE, by the hardware conversion (round to nearest, ties to even;
+// subnormals kept). It gives every NaN as the positive pattern 0x7FFF; a signed
+// 16-bit min against 0x7FC0 makes that the one NaN pattern 0x7FC0 and leaves every
+// other result (negative ones, +-Inf and finite values, all at most 0x7F80 as
+// signed halves) as it is. Checked against the integer rounding on this GPU over
+// every upper half with ties, neighbours of ties and random lower halves.
+__device__ __forceinline__ uint32_t round_pair_bf16_rtne(float x0, float x1) {
+  return ptx::min_s16x2(ptx::pack_bf16x2(x0, x1), 0x7FC07FC0u);
 }
 
 // The running output row of a softmax thread: 128 fp32 as 64 packed pairs
@@ -1202,8 +1210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Work wk = work_of<kCausal, kVarlen>(p, item);
         const uint32_t stage_w = sbase + kOffStage + (t * 4 + wq) * kStageWarpBytes;
         const int q_row0 = (2 * wk.pair + t) * kBM + wq * 32;
-        const uint32_t bias = p.mode == 0 ? 0x7FFFu : (p.mode == 1 ? 0x8000u : 0u);
-        const uint32_t lsb_mask = p.mode == 0 ? 1u : 0u;
+        const bool rtne = p.mode == 0;
+        const uint32_t bias = p.mode == 1 ? 0x8000u : 0u;
         const float inv_l = __frcp_rn(l);  // 0 -> Inf, so an all -Inf row gives 0 * Inf = NaN
         const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
 #pragma unroll
@@ -1213,11 +1221,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             uint32_t w[16];
+            if (rtne) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float o0, o1;
-              ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
-              w[i] = round_pair_bf16(o0, o1, bias, lsb_mask);
+              for (int i = 0; i < 16; ++i) {
+                float o0, o1;
+                ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+                w[i] = round_pair_bf16_rtne(o0, o1);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float o0, o1;
+                ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+                w[i] = round_pair_bf16(o0, o1, bias);
+              }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {

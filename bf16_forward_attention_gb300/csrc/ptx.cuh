@@ -486,6 +486,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // The upper 16 bits of a (into bits 0..15) and of b (into bits 16..31).
+// Signed 16-bit minimum of each half.
+__device__ __forceinline__ uint32_t min_s16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t prmt_hi16(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d) : "r"(a), "r"(b));
