@@ -79,9 +79,10 @@ int device_ready(int dev) {
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>),
-      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, false, true>)};
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, false, true>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true, false, true>)};
   for (const void* fn : variants) {
-    const bool persist = fn == variants[5];
+    const bool persist = fn == variants[5] || fn == variants[7];
     const bool pair = fn == variants[6];
     const bool row_limit = fn == variants[2] || fn == variants[3] || fn == variants[4];
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -322,9 +323,16 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
     attn::attn_fwd_kernel<false, true, false>
         <<<grid, attn::kThreads, attn::kSmemBytesRowLimit, cs>>>(tq, tk, tv, to, p);
   } else if (n_splits == 1 && p.kv_tiles <= kPersistMaxKvTiles && p.n_items > g_dev_sms[dev]) {
-    attn::attn_fwd_kernel<false, false, false, true>
-        <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
-            tq, tk, tv, to, p);
+    // One key tile of fewer than 128 keys per item: the short persistent variant,
+    // whose P V stops at the last 16-key chunk holding a key.
+    if (p.kv_tiles == 1 && p.kv_tail < attn::kBN)
+      attn::attn_fwd_kernel<false, false, false, true, false, true>
+          <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
+              tq, tk, tv, to, p);
+    else
+      attn::attn_fwd_kernel<false, false, false, true>
+          <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
+              tq, tk, tv, to, p);
   } else if (n_tail > 0) {
     // The full waves as usual, then the tail items as 2-CTA clusters, each with
     // its key range split in two halves and merged on chip (pair variant).

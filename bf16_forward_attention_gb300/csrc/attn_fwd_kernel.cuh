@@ -296,6 +296,21 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   issue_pv_seq(tmem_o, tmem_p, v_lo, accumulate, std::make_integer_sequence<int, 8>{});
 }
 
+// The same over the first n key chunks only (1 <= n <= 8): the one key tile of the
+// short persistent variant, whose P is written for the chunks that hold keys. A
+// rolled loop (a few instructions per chunk in the issuing thread).
+__device__ __forceinline__ void issue_pv_chunks(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
+                                                uint32_t accumulate, int n) {
+  constexpr uint32_t idesc = idesc_bf16(kBM, kD, 1);
+#pragma unroll 1
+  for (int k = 0; k < n; ++k) {
+    const uint32_t a = tmem_p + 16u * static_cast<uint32_t>(k);
+    const uint32_t b = v_lo + (static_cast<uint32_t>(k) << 7);
+    ptx::mma_ts_imm<0, 0>(tmem_o, a, b, kDescHi, idesc, k == 0 ? accumulate : 1u);
+    ptx::mma_ts_imm<8, 0>(tmem_o, a, b, kDescHi, idesc, 1u);
+  }
+}
+
 __device__ __forceinline__ uint32_t round_bf16_bits(float x, int mode) {
   uint32_t u = __float_as_uint(x);
   if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;  // NaN: one pattern
@@ -448,8 +463,12 @@ __device__ __forceinline__ void exp_chunk(uint32_t tS, int u, const uint32_t (&r
 }
 
 // Pass B over one key tile: exp, P split, row sum. The load of chunk u+1 is in
-// flight while chunk u is computed.
-template <bool kMasked>
+// flight while chunk u is computed. kSkipEmpty (the short persistent variant
+// only, where `valid` is the same for every row and the P V MMAs stop at the last
+// chunk holding a key): chunks wholly past `valid` are neither computed nor
+// written; the branch is uniform over the CTA, so the warp-collective TMEM stores
+// stay converged.
+template <bool kMasked, bool kSkipEmpty = false>
 __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float m_sub) {
   const uint64_t c2 = ptx::f2_pack(c, c);
   const uint64_t neg_m2 = ptx::f2_pack(-m_sub, -m_sub);
@@ -460,10 +479,10 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float
   for (int u = 0; u < 8; u += 2) {
     ptx::tmem_wait_ld16(ra);
     ptx::tmem_ld16_nowait(tS + 16 * (u + 1), rb);
-    exp_chunk<kMasked>(tS, u, ra, valid, c2, neg_m2, l);
+    if (!kSkipEmpty || 16 * u < valid) exp_chunk<kMasked>(tS, u, ra, valid, c2, neg_m2, l);
     ptx::tmem_wait_ld16(rb);
     if (u + 2 < 8) ptx::tmem_ld16_nowait(tS + 16 * (u + 2), ra);
-    exp_chunk<kMasked>(tS, u + 1, rb, valid, c2, neg_m2, l);
+    if (!kSkipEmpty || 16 * (u + 1) < valid) exp_chunk<kMasked>(tS, u + 1, rb, valid, c2, neg_m2, l);
   }
   float a0, a1, b0, b1;
   ptx::f2_unpack(l[0], a0, a1);
@@ -658,9 +677,11 @@ __device__ __forceinline__ int first_masked_tile(const Work& w) {
 // halves (n_splits = 2); rank 1 sends its unnormalised rows to rank 0 through
 // distributed shared memory, and rank 0 merges them with its own and stores
 // the output; used for the last, partial wave of a launch, which then takes half
-// the time. Each is compiled separately so that the other variants carry none
-// of it.
-template <bool kPartial, bool kCausal, bool kVarlen, bool kPersist = false, bool kPair = false>
+// the time. kShort (with kPersist): every item is one key tile holding fewer than
+// 128 keys; the P V MMAs and pass B stop at the last 16-key chunk holding a key.
+// Each is compiled separately so that the other variants carry none of it.
+template <bool kPartial, bool kCausal, bool kVarlen, bool kPersist = false, bool kPair = false,
+          bool kShort = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -677,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   static_assert(!kPersist || (!kPartial && !kCausal && !kVarlen), "persistent: base path only");
   static_assert(!kPair || (!kPartial && !kCausal && !kVarlen && !kPersist), "pair: base path only");
+  static_assert(!kShort || kPersist, "short: a persistent variant");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // A key limit per row (rising along the causal diagonal, or the sequence's
@@ -906,7 +928,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               ptx::tc_fence_after();
               const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
-              issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
+              // Short variant: P of the one (ragged) key tile was written for its first
+              // n_pv chunks only.
+              const int n_pv = (p.kv_tail + 15) >> 4;
+              if constexpr (kShort)
+                issue_pv_chunks(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o, n_pv);
+              else
+                issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
               if (!more) ptx::mma_commit(bar(kBarOFull + 0));
               if (more) {
                 if (!(ok = ring_wait(kit))) break;
@@ -919,7 +947,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   !(ok = wait_bounded(bar(kBarOFree + 1), (iter - 1) & 1, abort_flag, p.timeout_ns, true)))
                 break;
               ptx::tc_fence_after();
-              issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
+              if constexpr (kShort)
+                issue_pv_chunks(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o, n_pv);
+              else
+                issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
               ptx::mma_commit(bar(kBarKvEmpty + vit % kStages));
               if (!more) ptx::mma_commit(bar(kBarOFull + 1));
               if (more) {
@@ -1187,7 +1218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
             const bool masked_b = kRowLimit ? !(c > 0.f) : last;
             if (kRowLimit) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
-            l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
+            // Short variant (one ragged key tile per item): the chunks past the last
+            // key are skipped (the MMA issuer's P V stops at the last chunk holding
+            // a key).
+            static_assert(!kPersist || !kRowLimit, "one `valid` for every row");
+            l += masked_b ? tile_exp<true, kShort>(tS, valid, c, m_sub)
+                          : tile_exp<false>(tS, kBN, c, m_sub);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(kBarPFull + t));
