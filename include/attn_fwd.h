@@ -138,6 +138,8 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* out, int layo
  * Returns the count (>= 0), ATTN_ERR_INVALID_ARG if a size is below 1,
  * ATTN_ERR_TOO_LARGE beyond the launch limits of attn_fwd, or
  * ATTN_ERR_NO_DEVICE / ATTN_ERR_ARCH for the current device. Launches nothing.
+ * Neither this query nor ATTN_FLAG_SPLIT_TAIL has a counterpart on the pages:
+ * they concern how the work fills this GPU, not what is computed.
  */
 int attn_fwd_split_tail_items(int64_t B, int64_t Hq, int64_t Sq, int64_t Sk);
 

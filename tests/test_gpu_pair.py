@@ -175,3 +175,42 @@ def test_split_tail_items_where_the_flag_changes_nothing():
     assert attn.split_tail_items(1, 2 * sms, 256, 4000) == 0  # no partial wave
     assert attn.split_tail_items(1, sms - 1, 256, 4000) == 0  # a wave too large for pairs
     assert attn.split_tail_items(1, 4, 256, 1024) == 4        # 8 key tiles: one wave of pairs
+
+
+def test_split_tail_full_size_cross4k32k():
+    # The workload whose last wave the flag halves: 512 items, the last 56 of them
+    # (from head 28, query pair 8 on) on pairs. Those items must equal the
+    # full-size 2-way split and every other item the default call, bit for bit;
+    # sampled rows (most of them from the tail heads) go against the oracle.
+    import numpy as np
+    from oracle import attention_rows_fp64, bf16_bits_to_f64, to_bhsd
+
+    w = inputs.WORKLOADS["cross4k32k"]
+    n_qp = (w.Sq + 255) // 256
+    n_items = w.B * w.H * n_qp
+    n_tail = attn.split_tail_items(w.B, w.H, w.Sq, w.Sk)
+    assert 0 < n_tail < n_items
+    q, k, v = inputs.make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    tail = attn.attn_fwd_ex(qd, kd, vd, layout=w.layout, split_tail=True)
+    plain = attn.attn_fwd(qd, kd, vd, layout=w.layout)
+    split = attn.attn_fwd_splitkv(qd, kd, vd, num_splits=2, layout=w.layout)
+    torch.cuda.synchronize()
+    assert attn.attn_fwd_last_error() == attn.ATTN_OK
+    tb, pb, sb = (to_bhsd(bits_of(t), w.layout) for t in (tail, plain, split))
+    # Item of (b, h, row): pair + (b * H + h) * n_qp, rows of a pair 256 apart.
+    item = ((np.arange(w.B)[:, None, None] * w.H + np.arange(w.H)[None, :, None]) * n_qp
+            + (np.arange(w.Sq)[None, None, :] // 256))
+    in_tail = item >= n_items - n_tail
+    assert (tb[in_tail] == sb[in_tail]).all()
+    assert (tb[~in_tail] == pb[~in_tail]).all()
+    rng = np.random.default_rng(w.seed)
+    qb, kb, vb = (to_bhsd(t.view(torch.int16).numpy(), w.layout) for t in (q, k, v))
+    got, exact = [], []
+    for h in list(range(w.H - 5, w.H)) + [0, w.H // 2]:
+        rows = np.unique(np.concatenate([[0, 255, 256, 2047, 2048, w.Sq - 1],
+                                         rng.integers(0, w.Sq, 24)]))
+        exact.append(attention_rows_fp64(bf16_bits_to_f64(qb[0, h]), bf16_bits_to_f64(kb[0, h]),
+                                         bf16_bits_to_f64(vb[0, h]), inputs.default_scale(), rows))
+        got.append(tb[0, h, rows])
+    assert_parity(compare(np.concatenate(got), np.concatenate(exact), w.roundings[0]))
