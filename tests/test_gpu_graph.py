@@ -65,3 +65,47 @@ def test_graph_replay_equals_direct_calls():
         assert attn.attn_fwd_last_error() == attn.ATTN_OK
         assert torch.equal(out_ex.view(torch.int16), want_ex.view(torch.int16))
         assert torch.equal(out_split.view(torch.int16), want_split.view(torch.int16))
+
+
+def test_graph_replay_of_the_tail_split():
+    # ATTN_FLAG_SPLIT_TAIL: the full waves, then the tail items as 2-CTA clusters
+    # launched as a programmatic dependent of the full waves; and a call that is
+    # all pairs (one launch). Both captured in one graph and replayed.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = [(sms + 5, 256, 2100), (4, 256, 2100)]
+    assert [attn.split_tail_items(1, h, sq, sk) for h, sq, sk in shapes] == [5, 4]
+
+    def make(seed):
+        out = []
+        for i, (h, sq, sk) in enumerate(shapes):
+            q, k, v = inputs.make_qkv(inputs.Workload("gt", "bhsd", 1, h, sq, sk, seed=seed + i))
+            out.append((q.cuda(), k.cuda(), v.cuda()))
+        return out
+
+    bufs = [tuple(t.clone() for t in qkv) for qkv in make(1600)]
+    outs = [torch.empty_like(qkv[0]) for qkv in bufs]
+
+    def step():
+        for (q, k, v), o in zip(bufs, outs):
+            attn.attn_fwd_ex(q, k, v, layout="bhsd", out=o, split_tail=True)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in (1610, 1620):
+        fresh = make(seed)
+        for dst, src in zip(bufs, fresh):
+            for d, s_ in zip(dst, src):
+                d.copy_(s_)
+        graph.replay()
+        torch.cuda.synchronize()
+        wants = [attn.attn_fwd_ex(q, k, v, layout="bhsd", split_tail=True) for q, k, v in fresh]
+        torch.cuda.synchronize()
+        assert attn.attn_fwd_last_error() == attn.ATTN_OK
+        for o, want in zip(outs, wants):
+            assert torch.equal(o.view(torch.int16), want.view(torch.int16))
