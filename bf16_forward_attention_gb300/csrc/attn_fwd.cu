@@ -145,6 +145,8 @@ int device_ready(int dev) {
 // one-CTA-per-item launch) run on pairs; 0 if none. Problems that take the
 // persistent variant keep it.
 int64_t pair_tail_items(int dev, int64_t n_items, int64_t kv_tiles) {
+  // The pair launch numbers its CTAs' work items 2 * item + half in an int.
+  if (n_items > (int64_t(1) << 30) - 1) return 0;
   const int64_t sms = g_dev_sms[dev];
   if (kv_tiles <= kPersistMaxKvTiles && n_items > sms) return 0;
   const int64_t tail = n_items % sms;
