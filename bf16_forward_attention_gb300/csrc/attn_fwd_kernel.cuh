@@ -1441,7 +1441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kPair) {
           // The two halves of the key range: rank 1 sends, rank 0 merges. Row R of
           // the CTA (0..255) is 512 bytes of the ring at R * 512, its 16-byte chunk
-          // i at position i ^ (R & 31) (so a warp's 32 rows hit distinct banks).
+          // i at position i ^ (R & 31), so that the 8 rows of a quarter-warp's
+          // 16-byte accesses fall in distinct banks.
           const int R = t * kBM + row;
           const uint32_t row_s = sRing + static_cast<uint32_t>(R) * 512u;
           const uint32_t ml_s = sbase + kOffPairMl + static_cast<uint32_t>(R) * 8u;
