@@ -529,6 +529,71 @@ __device__ __forceinline__ void fold_last(uint32_t tO, Row& acc) {
   }
 }
 
+// The same when the row holds nothing yet (an item of one key tile): a load.
+__device__ __forceinline__ void load_last(uint32_t tO, Row& acc) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tO + 32 * ch, r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      acc[16 * ch + i] = ptx::f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+  }
+}
+
+// Both passes over the one key tile of an item of the short persistent variant
+// (valid = the tile's keys, 1..127, the same for every row, so every branch on it
+// is uniform): only the 16-key chunks holding a key are read, and the first five
+// (80 keys) are read from TMEM once and kept in registers for pass B, the output
+// row being dead until the epilogue (nothing precedes this tile); keeping six
+// spilled. Sets m_used as the first tile of an item does; returns the row sum.
+__device__ __forceinline__ float short_tile(uint32_t tS, int valid, float c, bool pos,
+                                            float& m_used) {
+  const float neg_inf = -__int_as_float(0x7F800000);
+  const float pos_inf = __int_as_float(0x7F800000);
+  uint32_t r[5][16];
+  float e0 = pos ? neg_inf : pos_inf, e1 = e0;
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    if (16 * ch >= valid) continue;
+    uint32_t q[16];
+    uint32_t (&x)[16] = ch < 5 ? r[ch < 5 ? ch : 0] : q;  // held, or read again in pass B
+    ptx::tmem_ld16_nowait(tS + 16 * ch, x);
+    ptx::tmem_wait_ld16(x);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      float s0 = __uint_as_float(x[i]), s1 = __uint_as_float(x[i + 1]);
+      if (16 * ch + i >= valid) s0 = pos ? neg_inf : pos_inf;
+      if (16 * ch + i + 1 >= valid) s1 = pos ? neg_inf : pos_inf;
+      if (pos) { e0 = ptx::max_nan(e0, s0); e1 = ptx::max_nan(e1, s1); }
+      else { e0 = ptx::min_nan(e0, s0); e1 = ptx::min_nan(e1, s1); }
+    }
+  }
+  const float ext = pos ? ptx::max_nan(e0, e1) : ptx::min_nan(e0, e1);
+  const float m_tile = ext * c;
+  if (m_tile > m_used + kTau) m_used = m_tile;
+  const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
+  const uint64_t c2 = ptx::f2_pack(c, c);
+  const uint64_t neg_m2 = ptx::f2_pack(-m_sub, -m_sub);
+  uint64_t l[2] = {0, 0};
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    if (16 * ch >= valid) continue;
+    if (ch < 5) {
+      exp_chunk<true>(tS, ch, r[ch < 5 ? ch : 0], valid, c2, neg_m2, l);
+    } else {
+      uint32_t q[16];
+      ptx::tmem_ld16_nowait(tS + 16 * ch, q);
+      ptx::tmem_wait_ld16(q);
+      exp_chunk<true>(tS, ch, q, valid, c2, neg_m2, l);
+    }
+  }
+  float a0, a1, b0, b1;
+  ptx::f2_unpack(l[0], a0, a1);
+  ptx::f2_unpack(l[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned long long timeout_ns) {
   const bool ok = wait_bounded(bar, parity, abort_flag, timeout_ns, true);
@@ -1132,12 +1197,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item < p.n_items) {
         m_used = neg_inf;
         l = 0.f;
+        // (The short variant loads the row from O at the end: it holds nothing before.)
+        if constexpr (!kShort) {
 #pragma unroll
-        for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+          for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+        }
         n_kv = work_of<kCausal, kVarlen>(p, item).n_kv;  // key tiles of this item
       }
       while (ok && item < p.n_items) {
-        {
+        if constexpr (kShort) {
+          // The item's one key tile: both passes from one read of S.
+          if (!(ok = warp_wait(bar(kBarSFull + t), sp, abort_flag, p.timeout_ns))) break;
+          ptx::tc_fence_after();
+          l = short_tile(tS, p.kv_tail, c, pos, m_used);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kBarPFull + t));
+        } else {
             if (!(ok = warp_wait(bar(kBarSFull + t), sp, abort_flag, p.timeout_ns))) break;
             ptx::tc_fence_after();
             // The ragged key tile is the last tile of the last split. Written as tests
@@ -1236,7 +1312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Fold the last partial into the row, then hand O back to the tensor pipe
         // (the next item's first P V overwrites it) before the stores.
         ptx::tc_fence_after();
-        fold_last(tO, acc);
+        if constexpr (kShort)
+          load_last(tO, acc);
+        else
+          fold_last(tO, acc);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarOFree + t));
         // Normalise, round, and store this warp's 32 rows with two TMA boxes (one
@@ -1294,8 +1373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (item < p.n_items) {
           m_used = neg_inf;
           l = 0.f;
+          if constexpr (!kShort) {
 #pragma unroll
-          for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+            for (int i = 0; i < kD / 2; ++i) acc[i] = 0;  // +0.0f in both halves
+          }
           n_kv = work_of<kCausal, kVarlen>(p, item).n_kv;  // key tiles of this item
         }
       }
