@@ -80,9 +80,10 @@ int device_ready(int dev) {
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>),
       reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, false, true>),
-      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true, false, true>)};
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true, false, 1>),
+      reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true, false, 2>)};
   for (const void* fn : variants) {
-    const bool persist = fn == variants[5] || fn == variants[7];
+    const bool persist = fn == variants[5] || fn == variants[7] || fn == variants[8];
     const bool pair = fn == variants[6];
     const bool row_limit = fn == variants[2] || fn == variants[3] || fn == variants[4];
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -325,10 +326,17 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, int la
     attn::attn_fwd_kernel<false, true, false>
         <<<grid, attn::kThreads, attn::kSmemBytesRowLimit, cs>>>(tq, tk, tv, to, p);
   } else if (n_splits == 1 && p.kv_tiles <= kPersistMaxKvTiles && p.n_items > g_dev_sms[dev]) {
-    // One key tile of fewer than 128 keys per item: the short persistent variant,
-    // whose P V stops at the last 16-key chunk holding a key.
+    // Items of at most 4 key tiles ending in a ragged one: a short persistent
+    // variant (the partial in TMEM until the epilogue, S kept in registers between
+    // the softmax passes, the ragged tile's P V cut at its last key chunk). One
+    // tile and 2 to 4 tiles are separate instantiations: the general form cost the
+    // one-tile case 4%.
     if (p.kv_tiles == 1 && p.kv_tail < attn::kBN)
-      attn::attn_fwd_kernel<false, false, false, true, false, true>
+      attn::attn_fwd_kernel<false, false, false, true, false, 1>
+          <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
+              tq, tk, tv, to, p);
+    else if (p.kv_tiles <= attn::kShortMaxKvTiles && p.kv_tail < attn::kBN)
+      attn::attn_fwd_kernel<false, false, false, true, false, 2>
           <<<static_cast<unsigned>(g_dev_sms[dev]), attn::kThreads, attn::kSmemBytesPersist, cs>>>(
               tq, tk, tv, to, p);
     else

@@ -79,6 +79,8 @@ constexpr float kTau = 8.0f;  // lazy-rescale threshold (factor 256)
 // (The split-KV variant once folded every tile; every 4 tiles measured 3-5%
 // faster on decode-like shapes.)
 constexpr int kFoldEvery = 4;
+// Items of at most this many key tiles never fold (the short persistent variant).
+constexpr int kShortMaxKvTiles = kFoldEvery;
 template <bool kPartial>
 constexpr int kFoldOf = kFoldEvery;
 
@@ -463,12 +465,8 @@ __device__ __forceinline__ void exp_chunk(uint32_t tS, int u, const uint32_t (&r
 }
 
 // Pass B over one key tile: exp, P split, row sum. The load of chunk u+1 is in
-// flight while chunk u is computed. kSkipEmpty (the short persistent variant
-// only, where `valid` is the same for every row and the P V MMAs stop at the last
-// chunk holding a key): chunks wholly past `valid` are neither computed nor
-// written; the branch is uniform over the CTA, so the warp-collective TMEM stores
-// stay converged.
-template <bool kMasked, bool kSkipEmpty = false>
+// flight while chunk u is computed.
+template <bool kMasked>
 __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float m_sub) {
   const uint64_t c2 = ptx::f2_pack(c, c);
   const uint64_t neg_m2 = ptx::f2_pack(-m_sub, -m_sub);
@@ -479,10 +477,10 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, int valid, float c, float
   for (int u = 0; u < 8; u += 2) {
     ptx::tmem_wait_ld16(ra);
     ptx::tmem_ld16_nowait(tS + 16 * (u + 1), rb);
-    if (!kSkipEmpty || 16 * u < valid) exp_chunk<kMasked>(tS, u, ra, valid, c2, neg_m2, l);
+    exp_chunk<kMasked>(tS, u, ra, valid, c2, neg_m2, l);
     ptx::tmem_wait_ld16(rb);
     if (u + 2 < 8) ptx::tmem_ld16_nowait(tS + 16 * (u + 2), ra);
-    if (!kSkipEmpty || 16 * (u + 1) < valid) exp_chunk<kMasked>(tS, u + 1, rb, valid, c2, neg_m2, l);
+    exp_chunk<kMasked>(tS, u + 1, rb, valid, c2, neg_m2, l);
   }
   float a0, a1, b0, b1;
   ptx::f2_unpack(l[0], a0, a1);
@@ -541,21 +539,25 @@ __device__ __forceinline__ void load_last(uint32_t tO, Row& acc) {
   }
 }
 
-// Both passes over the one key tile of an item of the short persistent variant
-// (valid = the tile's keys, 1..127, the same for every row, so every branch on it
-// is uniform): only the 16-key chunks holding a key are read, and the first five
-// (80 keys) are read from TMEM once and kept in registers for pass B, the output
-// row being dead until the epilogue (nothing precedes this tile); keeping six
-// spilled. Sets m_used as the first tile of an item does; returns the row sum.
+// Both passes over one key tile of an item of a short persistent variant (at
+// most 4 key tiles, so the output row stays in TMEM until the epilogue and its
+// registers are free during the softmax). kMasked: the ragged last tile, valid =
+// its keys (1..127, the same for every row, so every branch on it is uniform);
+// only the 16-key chunks holding a key are read. The first five chunks (80 keys)
+// are read from TMEM once and kept in registers for pass B; the others are read
+// again (keeping six spilled). Updates the row's reference m_used by the lazy rule
+// and sets f to the factor the row's earlier partial must take (1 if it did not
+// move); returns the tile's row sum, relative to the new reference.
+template <bool kMasked>
 __device__ __forceinline__ float short_tile(uint32_t tS, int valid, float c, bool pos,
-                                            float& m_used) {
+                                            float& m_used, float& f) {
   const float neg_inf = -__int_as_float(0x7F800000);
   const float pos_inf = __int_as_float(0x7F800000);
   uint32_t r[5][16];
   float e0 = pos ? neg_inf : pos_inf, e1 = e0;
 #pragma unroll
   for (int ch = 0; ch < 8; ++ch) {
-    if (16 * ch >= valid) continue;
+    if (kMasked && 16 * ch >= valid) continue;
     uint32_t q[16];
     uint32_t (&x)[16] = ch < 5 ? r[ch < 5 ? ch : 0] : q;  // held, or read again in pass B
     ptx::tmem_ld16_nowait(tS + 16 * ch, x);
@@ -563,29 +565,38 @@ __device__ __forceinline__ float short_tile(uint32_t tS, int valid, float c, boo
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
       float s0 = __uint_as_float(x[i]), s1 = __uint_as_float(x[i + 1]);
-      if (16 * ch + i >= valid) s0 = pos ? neg_inf : pos_inf;
-      if (16 * ch + i + 1 >= valid) s1 = pos ? neg_inf : pos_inf;
-      if (pos) { e0 = ptx::max_nan(e0, s0); e1 = ptx::max_nan(e1, s1); }
-      else { e0 = ptx::min_nan(e0, s0); e1 = ptx::min_nan(e1, s1); }
+      if (kMasked && 16 * ch + i >= valid) s0 = pos ? neg_inf : pos_inf;
+      if (kMasked && 16 * ch + i + 1 >= valid) s1 = pos ? neg_inf : pos_inf;
+      if (pos) {
+        e0 = ptx::max_nan(e0, s0);
+        e1 = ptx::max_nan(e1, s1);
+      } else {
+        e0 = ptx::min_nan(e0, s0);
+        e1 = ptx::min_nan(e1, s1);
+      }
     }
   }
   const float ext = pos ? ptx::max_nan(e0, e1) : ptx::min_nan(e0, e1);
   const float m_tile = ext * c;
-  if (m_tile > m_used + kTau) m_used = m_tile;
+  f = 1.f;
+  if (m_tile > m_used + kTau) {  // false for NaN
+    f = ptx::ex2(m_used - m_tile);  // 0 when m_used = -Inf
+    m_used = m_tile;
+  }
   const float m_sub = (m_used == neg_inf) ? 0.f : m_used;
   const uint64_t c2 = ptx::f2_pack(c, c);
   const uint64_t neg_m2 = ptx::f2_pack(-m_sub, -m_sub);
   uint64_t l[2] = {0, 0};
 #pragma unroll
   for (int ch = 0; ch < 8; ++ch) {
-    if (16 * ch >= valid) continue;
+    if (kMasked && 16 * ch >= valid) continue;
     if (ch < 5) {
-      exp_chunk<true>(tS, ch, r[ch < 5 ? ch : 0], valid, c2, neg_m2, l);
+      exp_chunk<kMasked>(tS, ch, r[ch < 5 ? ch : 0], valid, c2, neg_m2, l);
     } else {
       uint32_t q[16];
       ptx::tmem_ld16_nowait(tS + 16 * ch, q);
       ptx::tmem_wait_ld16(q);
-      exp_chunk<true>(tS, ch, q, valid, c2, neg_m2, l);
+      exp_chunk<kMasked>(tS, ch, q, valid, c2, neg_m2, l);
     }
   }
   float a0, a1, b0, b1;
@@ -742,11 +753,14 @@ __device__ __forceinline__ int first_masked_tile(const Work& w) {
 // halves (n_splits = 2); rank 1 sends its unnormalised rows to rank 0 through
 // distributed shared memory, and rank 0 merges them with its own and stores
 // the output; used for the last, partial wave of a launch, which then takes half
-// the time. kShort (with kPersist): every item is one key tile holding fewer than
-// 128 keys; the P V MMAs and pass B stop at the last 16-key chunk holding a key.
+// the time. kShort (with kPersist; the key range ends in a ragged tile): every
+// item has one key tile (1) or 2 to 4 (2), so its partial stays in TMEM until the
+// epilogue (no fold) and the softmax keeps S in the row's registers between its
+// two passes; on the ragged last tile the P V MMAs and pass B stop at the last
+// 16-key chunk holding a key.
 // Each is compiled separately so that the other variants carry none of it.
 template <bool kPartial, bool kCausal, bool kVarlen, bool kPersist = false, bool kPair = false,
-          bool kShort = false>
+          int kShort = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -763,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   static_assert(!kPersist || (!kPartial && !kCausal && !kVarlen), "persistent: base path only");
   static_assert(!kPair || (!kPartial && !kCausal && !kVarlen && !kPersist), "pair: base path only");
-  static_assert(!kShort || kPersist, "short: a persistent variant");
+  static_assert(kShort == 0 || (kPersist && kShort <= 2), "short: a persistent variant");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // A key limit per row (rising along the causal diagonal, or the sequence's
@@ -993,10 +1007,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               ptx::tc_fence_after();
               const uint32_t acc_o = (j % kFoldOf<kPartial>) != 0 ? 1u : 0u;  // partial continues
-              // Short variant: P of the one (ragged) key tile was written for its first
-              // n_pv chunks only.
-              const int n_pv = (p.kv_tail + 15) >> 4;
-              if constexpr (kShort)
+              // Short variants: P of the ragged last key tile was written for its first
+              // n_pv chunks only (kShort 1: every tile is that tile).
+              const int n_pv = (!more && p.kv_tail < kBN) ? (p.kv_tail + 15) >> 4 : 8;
+              if (kShort == 1 || (kShort == 2 && n_pv < 8))
                 issue_pv_chunks(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o, n_pv);
               else
                 issue_pv(tmem + kTmemO0, tmem + kTmemS0, v_desc(vit), acc_o);
@@ -1012,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   !(ok = wait_bounded(bar(kBarOFree + 1), (iter - 1) & 1, abort_flag, p.timeout_ns, true)))
                 break;
               ptx::tc_fence_after();
-              if constexpr (kShort)
+              if (kShort == 1 || (kShort == 2 && n_pv < 8))
                 issue_pv_chunks(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o, n_pv);
               else
                 issue_pv(tmem + kTmemO0 + 128, tmem + kTmemS0 + 128, v_desc(vit), acc_o);
@@ -1205,11 +1219,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_kv = work_of<kCausal, kVarlen>(p, item).n_kv;  // key tiles of this item
       }
       while (ok && item < p.n_items) {
-        if constexpr (kShort) {
+        if constexpr (kShort == 1) {
           // The item's one key tile: both passes from one read of S.
           if (!(ok = warp_wait(bar(kBarSFull + t), sp, abort_flag, p.timeout_ns))) break;
           ptx::tc_fence_after();
-          l = short_tile(tS, p.kv_tail, c, pos, m_used);
+          float f_row;
+          l = short_tile<true>(tS, p.kv_tail, c, pos, m_used, f_row);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(kBarPFull + t));
+        } else if constexpr (kShort == 2) {
+          // A key tile of an item of 2 to 4: both passes from one read of S. The
+          // item's partial stays in TMEM (no fold before the epilogue); when the
+          // reference moves, the partial of the earlier tiles is scaled there.
+          if (!(ok = warp_wait(bar(kBarSFull + t), sp, abort_flag, p.timeout_ns))) break;
+          ptx::tc_fence_after();
+          const bool last = (j == n_kv - 1) && (p.kv_tail < kBN);
+          float f_row;
+          const float l_tile = last ? short_tile<true>(tS, p.kv_tail, c, pos, m_used, f_row)
+                                    : short_tile<false>(tS, kBN, c, pos, m_used, f_row);
+          const bool need = f_row != 1.f;  // the reference moved (f < 2^-8, or 0)
+          if (need) l *= f_row;
+          l += l_tile;
+          if (j > 0 && __any_sync(0xFFFFFFFFu, need)) rescale_tmem_row(tO, f_row);
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar(kBarPFull + t));
@@ -1294,12 +1326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // no mask; for c <= 0 (where -Inf * c is not -Inf) it masks per element.
             const bool masked_b = kRowLimit ? !(c > 0.f) : last;
             if (kRowLimit) ptx::tmem_wait_st();  // pass A's write-backs before pass B reads
-            // Short variant (one ragged key tile per item): the chunks past the last
-            // key are skipped (the MMA issuer's P V stops at the last chunk holding
-            // a key).
-            static_assert(!kPersist || !kRowLimit, "one `valid` for every row");
-            l += masked_b ? tile_exp<true, kShort>(tS, valid, c, m_sub)
-                          : tile_exp<false>(tS, kBN, c, m_sub);
+            l += masked_b ? tile_exp<true>(tS, valid, c, m_sub) : tile_exp<false>(tS, kBN, c, m_sub);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(kBarPFull + t));

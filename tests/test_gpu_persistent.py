@@ -4,9 +4,11 @@ Whole-range problems with at most 16 key tiles and more work items (batch x
 head x pair of 128-row query tiles) than the GPU has SMs run one CTA per SM, each
 looping over its items with the barrier phases carried from one item to the next
 and the output stored through its own staging buffer. Every shape below takes
-that path; those whose items are one key tile of fewer than 128 keys take its
-short form, whose P V MMAs and exp pass stop at the last 16-key chunk holding a
-key. Whole tensors are compared, in both layouts and all rounding modes,
+that path; those whose items have at most 4 key tiles ending in a ragged one
+take one of its short forms (one tile, or 2 to 4), which keep the partial in
+TMEM until the epilogue and S in registers between the two softmax passes, and
+stop the P V MMAs and the exp pass at the last 16-key chunk holding a key.
+Whole tensors are compared, in both layouts and all rounding modes,
 with ragged query and key lengths, grouped-query heads, a NaN query, an infinite
 key and a negative scale. Reruns must be bit-identical.
 """
@@ -93,8 +95,8 @@ def test_persistent_specials_and_negative_scale():
 def test_persistent_equals_one_cta_per_item_bitwise(Sk):
     # Splitting the heads into calls of at most as many items as SMs keeps each
     # call on one CTA per item; results must match the persistent call bit for bit.
-    # 77 and 17 keys (one ragged key tile) take the short persistent variant, whose
-    # P V stops at the last 16-key chunk holding a key.
+    # 77 and 17 keys (one ragged key tile) take the one-tile short form, 300 keys
+    # (3 tiles, the last of 44 keys) the 2-to-4-tile short form.
     layout, B, H, Sq = "bhsd", 1, 240, 256
     q, k, v = (t.cuda() for t in _qkv(layout, B, H, H, Sq, Sk, seed=1400 + Sk))
     whole = attn.attn_fwd(q, k, v, layout=layout)
