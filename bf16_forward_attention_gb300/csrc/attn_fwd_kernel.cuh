@@ -1358,31 +1358,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t inv2 = ptx::f2_pack(inv_l, inv_l);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          if (lane == 0) ptx::bulk_wait_group_read_0();
-          __syncwarp();
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            uint32_t w[16];
+          if constexpr (kShort != 0) {
+            // Short forms: round this half of the row first, then wait until the
+            // previous box has been read out of the staging buffer (the rounding
+            // hides that wait), then write it. (The general persistent variant keeps
+            // the order below: its loop measured no gain from it.)
+            uint32_t w[32];
             if (rtne) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
+              for (int i = 0; i < 32; ++i) {
                 float o0, o1;
-                ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+                ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + i], inv2), o0, o1);
                 w[i] = round_pair_bf16_rtne(o0, o1);
               }
             } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
+              for (int i = 0; i < 32; ++i) {
                 float o0, o1;
-                ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+                ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + i], inv2), o0, o1);
                 w[i] = round_pair_bf16(o0, o1, bias);
               }
             }
+            if (lane == 0) ptx::bulk_wait_group_read_0();
+            __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int chunk = ch * 4 + u;
-              ptx::st_shared_v4(stage_w + lane * 128 + ((chunk ^ (lane & 7)) << 4), w[4 * u],
+            for (int u = 0; u < 8; ++u)
+              ptx::st_shared_v4(stage_w + lane * 128 + ((u ^ (lane & 7)) << 4), w[4 * u],
                                 w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+          } else {
+            if (lane == 0) ptx::bulk_wait_group_read_0();
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+              uint32_t w[16];
+              if (rtne) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  float o0, o1;
+                  ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+                  w[i] = round_pair_bf16_rtne(o0, o1);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  float o0, o1;
+                  ptx::f2_unpack(ptx::f2_mul(acc[32 * hf + 16 * ch + i], inv2), o0, o1);
+                  w[i] = round_pair_bf16(o0, o1, bias);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int chunk = ch * 4 + u;
+                ptx::st_shared_v4(stage_w + lane * 128 + ((chunk ^ (lane & 7)) << 4), w[4 * u],
+                                  w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+              }
             }
           }
           ptx::fence_proxy_async_smem();
