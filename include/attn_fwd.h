@@ -101,7 +101,9 @@ enum { ATTN_FLAG_CAUSAL = 1, ATTN_FLAG_SPLIT_TAIL = 2 };
  *   Hq, Hkv  query heads and key/value heads; Hq must be a multiple of Hkv, and
  *            query head h reads key/value head h / (Hq / Hkv). q and out have Hq
  *            heads, k and v have Hkv heads, all in `layout`.
- *   flags    0 or ATTN_FLAG_CAUSAL. Causal: key j is visible to query i iff
+ *   flags    0, or either or both of ATTN_FLAG_CAUSAL and ATTN_FLAG_SPLIT_TAIL
+ *            (any other bit: ATTN_ERR_UNSUPPORTED).
+ *            ATTN_FLAG_CAUSAL: key j is visible to query i iff
  *            j <= i + (Sk - Sq) (aligned at the bottom right, so the last query
  *            sees every key); hidden logits are -Inf, and a query that sees no
  *            key (possible when Sq > Sk) comes out NaN. Key tiles that no row of
@@ -263,18 +265,23 @@ const char* attn_status_str(int status);
  *                  Page-locked memory (cudaHostAlloc / cudaHostRegister) lets
  *                  the copies run asynchronously and overlap the kernels;
  *                  pageable memory works but the copies then serialise.
+ *   flags          0 or ATTN_FLAG_CAUSAL (ATTN_FLAG_SPLIT_TAIL or any other
+ *                  bit: ATTN_ERR_UNSUPPORTED).
  *   workspace      device memory of attn_fwd_host_workspace_bytes() bytes,
  *                  256-byte aligned, owned by the caller; it receives copies of
- *                  q, k, v and out in the same layout. Calls in flight at the
- *                  same time need separate workspaces.
+ *                  q, k, v and out, each chunk's share packed densely in
+ *                  `layout`. Calls in flight at the same time need separate
+ *                  workspaces.
  *   stream         the call is ordered after the work already on `stream`, and
  *                  later work on `stream` is ordered after all of it: `out` is
  *                  valid once `stream` has reached this point.
- * The problem is cut into up to 8 chunks that are contiguous in every tensor
- * (runs of heads for BHSD, runs of batch entries or of query rows for BSHD);
- * each chunk's upload, kernel (attn_fwd_ex on the sub-tensors) and download
- * run on internal streams ordered by events, so chunk i's kernel overlaps the
- * copies of its neighbours. Results are bit-identical to attn_fwd_ex.
+ * The problem is cut into up to 8 chunks: runs of heads for BHSD; for BSHD,
+ * runs of batch entries, or with fewer entries than chunks runs of key/value
+ * heads of each entry (strided on the host, copied with 2-D copies), or with a
+ * single key/value head runs of query rows. Each chunk's upload, kernel
+ * (attn_fwd_ex on the chunk's dense sub-tensors) and download run on internal
+ * streams ordered by events, so chunk i's kernel overlaps the copies of its
+ * neighbours. Results are bit-identical to attn_fwd_ex.
  * Errors: as attn_fwd_ex, and ATTN_ERR_INVALID_ARG for a missing or short
  * workspace, ATTN_ERR_MISALIGNED for a workspace not 256-byte aligned.
  */
