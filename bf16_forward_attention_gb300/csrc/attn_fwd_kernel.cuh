@@ -29,6 +29,15 @@
 // the next item's Q loads as soon as the current item's last S MMAs are done,
 // and each softmax warp stores its rows through a 4 KiB staging buffer of its
 // own rather than through the Q buffer.
+// Its short forms take items of one ragged key tile, or of 2 to 4 tiles ending
+// in a ragged one: each S tile is read from TMEM once into registers for both
+// softmax passes, the partial output stays in TMEM until the epilogue, and P V
+// and the exponentials stop at the last 16-key chunk that holds a key.
+//
+// The pair variant (opt-in, for the last, partial wave of a launch) runs each
+// item on a 2-CTA cluster, each CTA taking one half of the key tiles; the
+// second CTA sends its unnormalised rows, running max and row sum to the first
+// through distributed shared memory, and the first merges them and stores.
 //
 // Softmax is the online (running-max) form in base 2 with a lazy rescale: the
 // running output and row sum are rescaled only when a tile's max exceeds the max
