@@ -307,9 +307,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
   issue_pv_seq(tmem_o, tmem_p, v_lo, accumulate, std::make_integer_sequence<int, 8>{});
 }
 
-// The same over the first n key chunks only (1 <= n <= 8): the one key tile of the
-// short persistent variant, whose P is written for the chunks that hold keys. A
-// rolled loop (a few instructions per chunk in the issuing thread).
+// The same over the first n key chunks only (1 <= n <= 8): the ragged last key
+// tile of the short persistent forms, whose P is written for the chunks that
+// hold keys. A rolled loop (a few instructions per chunk in the issuing thread).
 __device__ __forceinline__ void issue_pv_chunks(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
                                                 uint32_t accumulate, int n) {
   constexpr uint32_t idesc = idesc_bf16(kBM, kD, 1);
@@ -554,7 +554,7 @@ __device__ __forceinline__ void load_last(uint32_t tO, Row& acc) {
 // its keys (1..127, the same for every row, so every branch on it is uniform);
 // only the 16-key chunks holding a key are read. The first five chunks (80 keys)
 // are read from TMEM once and kept in registers for pass B; the others are read
-// again (keeping six spilled). Updates the row's reference m_used by the lazy rule
+// again (holding a sixth chunk made the variant spill registers). Updates the row's reference m_used by the lazy rule
 // and sets f to the factor the row's earlier partial must take (1 if it did not
 // move); returns the tile's row sum, relative to the new reference.
 template <bool kMasked>
